@@ -1,0 +1,120 @@
+"""MoE layer forward, plainly (test infrastructure; see ``oracle/__init__``).
+
+Two independent formulations of the same sum, both in float64 with no
+intermediate rounding:
+
+* ``expert_loop_forward`` -- the "expert view" of the mini-sglang MoE chapter
+  (``TorchMoeBackend.forward``): for every selected expert, gather its tokens,
+  run the SwiGLU MLP, scale by the route weight and add back into the tokens'
+  rows;
+* ``token_view_forward`` -- the "token view" of "Fused MoE Part 3" (section
+  01, ``selected_weights = weight[topk_ids]``): every token is projected by the
+  weights of its own selected experts, one (token, slot) pair at a time.
+
+Weight layout follows the mini-sglang ``MoELayer``: ``w1`` (gate_up_proj) is
+[E, 2I, H] with the gate rows first ([0, I)) and the up rows second ([I, 2I));
+``w2`` (down_proj) is [E, H, I]. SwiGLU is ``silu(gate) * up`` (the chapter's
+``silu_and_mul`` and its third exercise). The route weights stay in float64
+(the page casts them to the activation dtype; the reading here keeps them
+exact).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import routing
+
+
+def silu(v: np.ndarray) -> np.ndarray:
+    return v / (1.0 + np.exp(-v))
+
+
+def expert_projection(x: np.ndarray, weight: np.ndarray, topk_ids: np.ndarray) -> np.ndarray:
+    """Fused MoE Part 3, section 03 task: output[m, j, :] = x[m] @ weight[topk_ids[m, j]]^T.
+
+    x [M, K], weight [E, N, K], topk_ids [M, topk] -> [M, topk, N] (float64).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    weight = np.asarray(weight, dtype=np.float64)
+    ids = np.asarray(topk_ids)
+    M, topk = ids.shape
+    out = np.zeros((M, topk, weight.shape[1]))
+    for m in range(M):
+        for j in range(topk):
+            out[m, j] = weight[ids[m, j]] @ x[m]
+    return out
+
+
+def expert_loop_forward(x, w1, w2, topk_weights, topk_ids) -> np.ndarray:
+    """Expert view (mini-sglang TorchMoeBackend): y [T, H] float64."""
+    x = np.asarray(x, dtype=np.float64)
+    w1 = np.asarray(w1, dtype=np.float64)
+    w2 = np.asarray(w2, dtype=np.float64)
+    I = w1.shape[1] // 2
+    T, topk = np.asarray(topk_ids).shape
+    flat_ids = np.asarray(topk_ids).reshape(-1)
+    flat_w = np.asarray(topk_weights, dtype=np.float64).reshape(-1)
+    token_of_pair = np.repeat(np.arange(T), topk)
+    out = np.zeros_like(x)
+    for e in np.unique(flat_ids):
+        sel = np.nonzero(flat_ids == e)[0]
+        tokens = token_of_pair[sel]
+        xs = x[tokens]
+        gate = xs @ w1[e, :I].T
+        up = xs @ w1[e, I:].T
+        h = silu(gate) * up
+        y = (h @ w2[e].T) * flat_w[sel][:, None]
+        np.add.at(out, tokens, y)
+    return out
+
+
+def token_view_forward(x, w1, w2, topk_weights, topk_ids) -> np.ndarray:
+    """Token view: for every token t and slot j, y[t] += w[t,j] * down(swiglu(gate_up(x_t))).
+
+    Uses ``expert_projection`` for the gathered gate_up projection. Python loops
+    over (token, slot): small cases only.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    w2 = np.asarray(w2, dtype=np.float64)
+    ids = np.asarray(topk_ids)
+    tw = np.asarray(topk_weights, dtype=np.float64)
+    I = np.asarray(w1).shape[1] // 2
+    gu = expert_projection(x, w1, ids)                  # [T, topk, 2I]
+    h = silu(gu[:, :, :I]) * gu[:, :, I:]               # [T, topk, I]
+    T, topk = ids.shape
+    out = np.zeros((T, w2.shape[1]))
+    for t in range(T):
+        for j in range(topk):
+            out[t] += tw[t, j] * (w2[ids[t, j]] @ h[t, j])
+    return out
+
+
+def fused_forward(x, gating_output, w1, w2, topk: int, renormalize: bool,
+                  num_expert_group: int = 1, topk_group: int = 1, scoring_func: str = "softmax",
+                  routed_scaling_factor: float = 1.0):
+    """The whole layer: grouped top-k routing, then the expert-loop MoE.
+
+    Returns (y float64 [T, H], topk_weights float32, topk_ids int32). The float32
+    route weights (the routing output) are the ones the MoE sums with.
+    """
+    tw, ids = routing.grouped_topk(gating_output, topk, renormalize, num_expert_group,
+                                   topk_group, scoring_func, routed_scaling_factor)
+    y = expert_loop_forward(x, w1, w2, tw, ids)
+    return y, tw, ids
+
+
+def token_outputs(x_rows, w1_experts, w2_experts, weights) -> np.ndarray:
+    """One token's output from its own experts: sum_j w_j * W2_j (silu(G_j x) * U_j x).
+
+    ``x_rows`` [H]; ``w1_experts`` list of [2I, H]; ``w2_experts`` list of [H, I];
+    ``weights`` [topk]. Used to check sampled tokens of workloads too large for
+    the full oracle.
+    """
+    x = np.asarray(x_rows, dtype=np.float64)
+    out = 0.0
+    for w1e, w2e, wj in zip(w1_experts, w2_experts, weights):
+        w1e = np.asarray(w1e, dtype=np.float64)
+        I = w1e.shape[0] // 2
+        h = silu(w1e[:I] @ x) * (w1e[I:] @ x)
+        out = out + float(wj) * (np.asarray(w2e, dtype=np.float64) @ h)
+    return out
