@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 fused MoE layer forward.
+
+Default workload: the prefill layer T=4096, H=2048, I=768, E=128, top-8 softmax
+routing with renormalisation (bf16 activations and weights). A step is one full
+pass of the hot path through the C ABI (moe_fused_forward: routing, align,
+gate_up grouped GEMM + SwiGLU, down grouped GEMM + weighted combine, cast).
+Inputs are resident in HBM when the timed region starts; L2 is flushed (256 MiB
+write) between timed steps, outside the per-step CUDA-event windows.
+
+Also reported: the decode layer (E=256, H=7168, I=2048, grouped sigmoid routing)
+as weight-stream GB/s at T in {1, 8, 32, 128}, and grouped top-k routing alone
+at T=16384 as GB/s. `--impl reference` times the CPU oracle instead.
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import pathlib
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = pathlib.Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "MoE layer tokens/s + % BF16 tensor peak; decode weight-stream GB/s vs HBM"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = ROOT / "gpurun_out" / f"clocks_rank{gpu_index}.csv"
+
+    def start(self):
+        try:
+            self.path.parent.mkdir(exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.path.read_text().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- helpers
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    d = json.loads(p.read_text()).get(kernel)
+    if not d:
+        return None
+    src = ROOT / d["source"]
+    if not src.exists() or hashlib.sha256(src.read_bytes()).hexdigest() != d["source_sha256"]:
+        return None
+    return d["bytes_per_launch"]
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def oracle_layer_step(cfg, x64, g32, w1_64, w2_64):
+    from oracle import moe as omoe
+    return omoe.fused_forward(x64, g32, w1_64, w2_64, cfg.topk, cfg.renormalize, cfg.num_expert_group,
+                              cfg.topk_group, cfg.scoring, cfg.routed_scaling_factor)
+
+
+def oracle_inputs(cfg, n_tokens):
+    """float64 copies of the workload's first n_tokens tokens and all expert weights (generated on the host)."""
+    import numpy as np
+    import synth
+    import torch
+    acts = synth.moe_activations(synth.MoEConfig(**{**cfg.__dict__, "T": n_tokens}), "cpu")
+    W = synth.moe_weights(cfg, "cuda" if torch.cuda.is_available() else "cpu")
+    w1 = W["w1"].float().cpu().numpy().astype(np.float64)
+    w2 = W["w2"].float().cpu().numpy().astype(np.float64)
+    del W
+    return acts["x"].float().numpy().astype(np.float64), acts["gating"].numpy(), w1, w2
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
+    import torch
+    import mixture_experts_routing_grouped_gb300 as moe
+    import synth
+
+    from mixture_experts_routing_grouped_gb300 import build as _b
+    _b.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = synth.prefill_config()
+    acts = synth.moe_activations(cfg, dev)
+    W = synth.moe_weights(cfg, dev)
+    ws = torch.zeros(moe.moe_fused_forward_workspace_size(cfg.T, cfg.H, cfg.I, cfg.E, cfg.topk), dtype=torch.uint8,
+                     device=dev)
+    y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    tw = torch.empty((cfg.T, cfg.topk), dtype=torch.float32, device=dev)
+    ids = torch.empty((cfg.T, cfg.topk), dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(x, g, yy, w_, i_):
+        moe.moe_fused_forward(x, g, W["w1"], W["w2"], cfg.topk, cfg.renormalize, cfg.num_expert_group,
+                              cfg.topk_group, cfg.scoring, cfg.routed_scaling_factor, ws=ws, y=yy, topk_weights=w_,
+                              topk_ids=i_)
+
+    n_stage = 7
+    for _ in range(args.warmup):
+        step(acts["x"], acts["gating"], y, tw, ids)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage)] for _ in range(K)]
+    s = torch.cuda.current_stream()
+    for row in ev:                    # create the event handles before handing them to the library
+        for e in row:
+            e.record(s)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for k in range(K):
+        flush.fill_(float(k))
+        moe.moe_set_stage_events(ev[k])
+        step(acts["x"], acts["gating"], y, tw, ids)
+        moe.moe_set_stage_events(None)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [ev[k][0].elapsed_time(ev[k][n_stage - 1]) for k in range(K)]
+    stage_names = ["routing", "align", "acc_clear", "gemm_gate_up", "gemm_down", "cast"]
+    stage_ms = {n: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
+                for i, n in enumerate(stage_names)}
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    err = moe.moe_check_device_error(ws)
+    if err:
+        raise RuntimeError(f"device error word {err:#x}")
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    xh = acts["x"].cpu().pin_memory()
+    gh = acts["gating"].cpu().pin_memory()
+    yh = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    twh = torch.empty((cfg.T, cfg.topk), dtype=torch.float32).pin_memory()
+    idh = torch.empty((cfg.T, cfg.topk), dtype=torch.int32).pin_memory()
+    xd, gd = torch.empty_like(acts["x"]), torch.empty_like(acts["gating"])
+    e2e = []
+    for k in range(args.warmup + K):
+        flush.fill_(float(k))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        xd.copy_(xh, non_blocking=True)
+        gd.copy_(gh, non_blocking=True)
+        step(xd, gd, y, tw, ids)
+        yh.copy_(y, non_blocking=True)
+        twh.copy_(tw, non_blocking=True)
+        idh.copy_(ids, non_blocking=True)
+        b.record()
+        b.synchronize()
+        if k >= args.warmup:
+            e2e.append(a.elapsed_time(b))
+    e2e_ms = statistics.mean(e2e)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = xh.numel() * 2 + gh.numel() * 4
+    d2h = yh.numel() * 2 + twh.numel() * 4 + idh.numel() * 4
+
+    # ---- roofline of the dominant kernel (gate_up grouped GEMM)
+    pairs = cfg.T * cfg.topk
+    flops_gate_up = 2.0 * pairs * cfg.H * (2 * cfg.I)
+    flops_down = 2.0 * pairs * cfg.I * cfg.H
+    t_gu = stage_ms["gemm_gate_up"] * 1e-3
+    achieved = flops_gate_up / t_gu / 1e12
+    peak = float(peaks["bf16_tflops"])
+    layer_tflops = (flops_gate_up + flops_down) / (ms * 1e-3) / 1e12
+
+    result = {
+        "metric": METRIC,
+        "value": round(world * cfg.T / (ms * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded counter-based normal inputs, random-init expert weights)",
+        "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "topk": cfg.topk,
+                   "routing": "softmax, renormalize, G=1", "l2": "256 MiB flush write between timed steps",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "moe_gemm_kernel<gate_up>", "bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"bf16_tflops (burst) of {peaks_kind}",
+                     "traffic": kernel_traffic("moe_gemm_kernel<gate_up>")},
+        "layer_tflops": round(layer_tflops, 1),
+        "layer_frac_bf16_peak": round(layer_tflops / peak, 4),
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "e2e": {"value": round(world * cfg.T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 6 * K,
+        "clocks": clk,
+    }
+    if not args.skip_extra and world == 1:
+        result["decode"] = bench_decode(moe, synth, torch, dev, flush, peaks, args)
+        result["routing"] = bench_routing(moe, synth, torch, dev, flush, peaks, args)
+    del W
+    return result, cfg
+
+
+def bench_decode(moe, synth, torch, dev, flush, peaks, args):
+    """Decode layer at T in {1, 8, 32, 128}: weight-stream GB/s = bytes of the active experts / step time."""
+    import numpy as np
+    out = {}
+    cfg0 = synth.decode_config(1)
+    W = synth.moe_weights(cfg0, dev)
+    for T in (1, 8, 32, 128):
+        cfg = synth.decode_config(T)
+        acts = synth.moe_activations(cfg, dev)
+        ws = torch.zeros(moe.moe_fused_forward_workspace_size(T, cfg.H, cfg.I, cfg.E, cfg.topk),
+                         dtype=torch.uint8, device=dev)
+        run = lambda: moe.moe_fused_forward(acts["x"], acts["gating"], W["w1"], W["w2"], cfg.topk, cfg.renormalize,
+                                            cfg.num_expert_group, cfg.topk_group, cfg.scoring,
+                                            cfg.routed_scaling_factor, ws=ws)
+        for _ in range(3):
+            _, _, ids = run()
+        torch.cuda.synchronize()
+        n_active = int(np.unique(ids.cpu().numpy()).size)
+        times = []
+        for k in range(max(5, args.steps)):
+            flush.fill_(float(k))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            run()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.mean(times)
+        wbytes = n_active * 3 * cfg.I * cfg.H * 2
+        gbs = wbytes / (ms * 1e-3) / 1e9
+        out[f"T{T}"] = {"ms": round(ms, 4), "active_experts": n_active, "weight_bytes": wbytes,
+                        "GB/s": round(gbs, 1), "frac_hbm": round(gbs / float(peaks["hbm_gbs"]), 4),
+                        "tokens/s": round(T / (ms * 1e-3), 1)}
+    del W
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_routing(moe, synth, torch, dev, flush, peaks, args):
+    out = {}
+    for T in (16384, 65536):
+        cfg = synth.routing_config(T, "sigmoid")
+        g = synth.gating_logits(cfg, dev)
+        w = torch.empty((T, cfg.topk), dtype=torch.float32, device=dev)
+        i = torch.empty((T, cfg.topk), dtype=torch.int32, device=dev)
+        run = lambda: moe.moe_grouped_topk(g, cfg.topk, True, cfg.num_expert_group, cfg.topk_group, cfg.scoring,
+                                           cfg.routed_scaling_factor, w, i)
+        for _ in range(3):
+            run()
+        times = []
+        for k in range(max(10, args.steps)):
+            flush.fill_(float(k))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            run()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        us = statistics.mean(times) * 1e3
+        nbytes = T * cfg.E * 4 + T * cfg.topk * 8
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[f"T{T}"] = {"us": round(us, 2), "bytes": nbytes, "GB/s": round(gbs, 1),
+                        "frac_hbm": round(gbs / float(peaks["hbm_gbs"]), 4)}
+    return out
+
+
+# --------------------------------------------------------------------------- CPU baseline / reference arm
+def cpu_baseline(cfg, budget_s: float = 12.0):
+    """Times the oracle on the first n tokens of the workload, doubling n until a run takes ~budget_s/4."""
+    n, last = 128, None
+    x64, g32, w1, w2 = oracle_inputs(cfg, cfg.T)
+    while True:
+        t0 = time.perf_counter()
+        oracle_layer_step(cfg, x64[:n], g32[:n], w1, w2)
+        dt = time.perf_counter() - t0
+        last = (n, dt)
+        if dt > budget_s / 4 or n >= cfg.T:
+            break
+        n = min(cfg.T, n * 2)
+    n, dt = last
+    return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"first {n} of {cfg.T} tokens of {cfg.name} (all {cfg.E} experts' weights), float64 numpy, "
+                      f"one run of {dt:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    import synth
+    cfg = synth.prefill_config()
+    n = 256
+    x64, g32, w1, w2 = oracle_inputs(cfg, n)
+    for _ in range(args.warmup):
+        oracle_layer_step(cfg, x64, g32, w1, w2)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_layer_step(cfg, x64, g32, w1, w2)
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    val = round(n / (ms * 1e-3), 2)
+    return {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs as the GPU arm)",
+        "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "topk": cfg.topk,
+                   "sample_tokens_per_step": n},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"first {n} of {cfg.T} tokens per step, float64 numpy oracle"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--skip-extra", action="store_true", help="skip the decode and routing sub-benchmarks")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, world, local_rank = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    peaks, kind = load_peaks()
+    result, cfg = run_ours(args, peaks, kind, rank, world, local_rank)
+    if rank == 0:
+        if not args.skip_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(cfg)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,62 @@
+// Host-side services shared by every entry point: device attributes, launch
+// status, kernel attributes, the device error word and status names.
+#include "common.cuh"
+
+#include <mutex>
+#include <set>
+#include <utility>
+
+namespace moe {
+
+int num_sms() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> g(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+moe_status_t launch_status() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool ensure_smem_attr(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> g(mu);
+  if (done.count({func, dev})) return true;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  done.insert({func, dev});
+  return true;
+}
+
+}  // namespace moe
+
+extern "C" moe_status_t moe_check_device_error(void* ws, int* code, void* stream) {
+  if (!ws || !code) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = moe::as_stream(stream);
+  int host = 0;
+  if (cudaMemcpyAsync(&host, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  *code = host;
+  return host == 0 ? MOE_OK : MOE_ERR_DEVICE_DATA;
+}
+
+extern "C" const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_DATA: return "MOE_ERR_DEVICE_DATA";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}

@@ -1,0 +1,41 @@
+// Shared host/device helpers of the MoE library (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <cstddef>
+
+#include "moe_gb300.h"
+
+namespace moe {
+
+constexpr int kWarp = 32;
+
+// Workspace header: the first 256 bytes of every workspace.
+//   [0]   int32 device error word (MOE_DEVERR_* bits)
+//   [4..] int32 scratch counters used by the kernels of one call
+constexpr size_t kWsHeader = 256;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Records a device-side data error without trapping.
+__device__ inline void report_error(int* err, int bits) {
+  if (err) atomicOr(err, bits);
+}
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+moe_status_t launch_status();
+
+// Raises a kernel's dynamic shared memory limit once per (kernel, device).
+bool ensure_smem_attr(const void* func, int bytes);
+
+}  // namespace moe

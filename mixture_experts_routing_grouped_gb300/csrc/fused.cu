@@ -1,0 +1,151 @@
+// moe_fused_forward: the routed MoE layer on one stream.
+//
+// Follows the mini-sglang MoE chapter, FusedMoeBackend.forward: routing
+// (select_experts, here the grouped top-k), moe_align_block_size, the gate_up
+// grouped GEMM (rows gathered as pair / topk), silu(gate) * up, the down grouped
+// GEMM multiplied by the route weight, and the sum over the topk slots of every
+// token. The page's intermediate buffers cache1..cache3 ([T*k, 2I], [T*k, I],
+// [T*k, H]) are replaced by h = silu(gate) * up in sorted order (written once by
+// the gate_up epilogue, read once by the down GEMM) and an fp32 [T, H]
+// accumulator that the down epilogue adds into; the page's host synchronisation
+// on the padded length is replaced by a device-side length read by the GEMMs.
+#include "common.cuh"
+
+namespace moe {
+
+moe_status_t validate_routing(int T, int E, int G, int kg, int k, int scoring);
+moe_status_t launch_grouped_topk(const float* gating, int T, int E, int G, int kg, int k, int scoring, int renorm,
+                                 float rsf, float* w, int32_t* ids, cudaStream_t s);
+size_t align_max_padded(int num_pairs, int E, int block_m);
+moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m, int32_t* sorted_ids,
+                          int32_t* expert_ids, int32_t* expert_offsets, int32_t* ntpp, int* err, cudaStream_t s);
+moe_status_t launch_gemm_gate_up(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_ids,
+                                 const int32_t* expert_ids, const int32_t* ntpp, __nv_bfloat16* h, int* err,
+                                 int num_pairs, int topk, int H, int I, int E, cudaStream_t s);
+moe_status_t launch_gemm_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, const int32_t* sorted_ids,
+                              const int32_t* expert_ids, const int32_t* ntpp, const float* topk_w, float* y_acc,
+                              int* err, int num_pairs, int topk, int cap, int H, int I, int E, cudaStream_t s);
+
+namespace {
+
+constexpr int kBlockM = 128;
+
+__global__ void zero_f32_kernel(float4* __restrict__ p, size_t n4) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__global__ void cast_f32_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float4 v = src[i];
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    dst[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  }
+}
+
+struct FusedLayout {
+  size_t sorted_ids, expert_ids, expert_offsets, ntpp, h, y_acc, total;
+  int cap;
+};
+
+FusedLayout fused_layout(int T, int H, int I, int E, int topk) {
+  FusedLayout L{};
+  const int num_pairs = T * topk;
+  L.cap = static_cast<int>(align_max_padded(num_pairs, E, kBlockM));
+  size_t off = kWsHeader;
+  L.sorted_ids = off; off = align_up(off + static_cast<size_t>(L.cap) * 4, 256);
+  L.expert_ids = off; off = align_up(off + static_cast<size_t>(L.cap / kBlockM + 1) * 4, 256);
+  L.expert_offsets = off; off = align_up(off + static_cast<size_t>(E + 1) * 4, 256);
+  L.ntpp = off; off = align_up(off + 4, 1024);
+  L.h = off; off = align_up(off + static_cast<size_t>(L.cap) * I * 2, 1024);
+  L.y_acc = off; off = align_up(off + static_cast<size_t>(T) * H * 4, 256);
+  L.total = off;
+  return L;
+}
+
+thread_local cudaEvent_t g_stage_events[8];
+thread_local int g_num_stage_events = 0;
+
+inline void stage_mark(int i, cudaStream_t s) {
+  if (i < g_num_stage_events) cudaEventRecord(g_stage_events[i], s);
+}
+
+int grid_for(size_t n4) {
+  const size_t want = (n4 + 255) / 256;
+  const size_t cap = static_cast<size_t>(num_sms() > 0 ? num_sms() : 148) * 8;
+  return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" void moe_set_stage_events(void* const* events, int n) {
+  moe::g_num_stage_events = (events && n > 0) ? (n < 8 ? n : 8) : 0;
+  for (int i = 0; i < moe::g_num_stage_events; ++i) moe::g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+}
+
+extern "C" size_t moe_fused_forward_workspace_size(int T, int H, int I, int E, int topk) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0) return 0;
+  return moe::fused_layout(T, H, I, E, topk).total;
+}
+
+extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, const void* w_gate_up,
+                                          const void* w_down, int T, int H, int I, int E, int num_expert_group,
+                                          int topk_group, int topk, int scoring, int renormalize,
+                                          float routed_scaling_factor, void* y, float* topk_weights,
+                                          int32_t* topk_ids, void* ws, size_t ws_bytes, void* stream) {
+  using namespace moe;
+  moe_status_t st = validate_routing(T, E, num_expert_group, topk_group, topk, scoring);
+  if (st != MOE_OK) return st;
+  if (H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+  if (!w_gate_up || !w_down) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !gating || !y || !topk_weights || !topk_ids)) return MOE_ERR_INVALID_ARG;
+  if (H % 256 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(gating) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y))
+    return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (static_cast<long long>(T) * topk >= (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  const FusedLayout L = fused_layout(T, H, I, E, topk);
+  if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+
+  cudaStream_t s = as_stream(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* err = reinterpret_cast<int*>(w);
+  int32_t* sorted_ids = reinterpret_cast<int32_t*>(w + L.sorted_ids);
+  int32_t* expert_ids = reinterpret_cast<int32_t*>(w + L.expert_ids);
+  int32_t* offsets = reinterpret_cast<int32_t*>(w + L.expert_offsets);
+  int32_t* ntpp = reinterpret_cast<int32_t*>(w + L.ntpp);
+  __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(w + L.h);
+  float* y_acc = reinterpret_cast<float*>(w + L.y_acc);
+  const int num_pairs = T * topk;
+
+  stage_mark(0, s);
+  st = launch_grouped_topk(gating, T, E, num_expert_group, topk_group, topk, scoring, renormalize,
+                           routed_scaling_factor, topk_weights, topk_ids, s);
+  if (st != MOE_OK) return st;
+  stage_mark(1, s);
+  st = launch_align(topk_ids, num_pairs, E, kBlockM, sorted_ids, expert_ids, offsets, ntpp, err, s);
+  if (st != MOE_OK) return st;
+  stage_mark(2, s);
+  const size_t n4 = static_cast<size_t>(T) * H / 4;
+  zero_f32_kernel<<<grid_for(n4), 256, 0, s>>>(reinterpret_cast<float4*>(y_acc), n4);
+  if ((st = launch_status()) != MOE_OK) return st;
+  stage_mark(3, s);
+  st = launch_gemm_gate_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_gate_up),
+                           sorted_ids, expert_ids, ntpp, h, err, num_pairs, topk, H, I, E, s);
+  if (st != MOE_OK) return st;
+  stage_mark(4, s);
+  st = launch_gemm_down(h, static_cast<const __nv_bfloat16*>(w_down), sorted_ids, expert_ids, ntpp, topk_weights,
+                        y_acc, err, num_pairs, topk, L.cap, H, I, E, s);
+  if (st != MOE_OK) return st;
+  stage_mark(5, s);
+  cast_f32_bf16_kernel<<<grid_for(n4), 256, 0, s>>>(reinterpret_cast<const float4*>(y_acc),
+                                                    reinterpret_cast<uint2*>(y), n4);
+  if ((st = launch_status()) != MOE_OK) return st;
+  stage_mark(6, s);
+  return MOE_OK;
+}

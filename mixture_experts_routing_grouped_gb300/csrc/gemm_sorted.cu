@@ -1,0 +1,364 @@
+// Grouped GEMMs of the MoE layer over the expert-sorted, BLOCK_M-padded pair
+// layout, on tcgen05 tensor cores with TMEM accumulators.
+//
+// Follows the mini-sglang MoE chapter ("fused MoE", fused_moe_kernel and
+// FusedMoeBackend.forward): every 128-row block of the sorted layout belongs to
+// one expert (expert_ids), its rows are the pairs sorted_token_ids[...], and
+//   gate_up pass: C[row] = X[pair / topk] @ W1[e]^T   (rows gathered in-kernel)
+//   down pass:    C[row] = h[row] @ W2[e]^T, scaled by the route weight and
+//                 summed into the pair's token row.
+// The SwiGLU of the chapter's third exercise is fused into the gate_up
+// epilogue: the B tile stacks 128 gate rows [n0, n0+128) over the matching 128
+// up rows [I+n0, I+n0+128), so each accumulator row holds the paired gate and
+// up columns and one thread writes h = silu(gate) * up directly. No
+// weight[topk_ids] and no permuted copy of X exist ("Fused MoE Part 3",
+// section 01): the gather happens while staging A into shared memory.
+//
+// Kernel shape (one persistent CTA per SM, 288 threads):
+//   warps 0-3  epilogue: TMEM -> registers -> global (TMEM lane quarter = warp)
+//   warps 4-7  producers: cp.async gather of A rows (gate_up pass), TMA for B
+//              (and for A in the down pass), 4-stage shared-memory ring
+//   warp 8     TMEM allocation and the single MMA-issuing thread
+// The 128 x 256 fp32 accumulator lives in TMEM, double-buffered (512 columns)
+// so that the epilogue of one tile overlaps the main loop of the next.
+// Tiles (m-block, n-block) are taken round-robin with the n-block fastest, so
+// the CTAs working at one time share each expert's weight tiles through L2.
+#include "common.cuh"
+#include "ptx.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+namespace moe {
+
+constexpr int kBM = 128;          // rows per tile (= align block_m)
+constexpr int kBN = 256;          // accumulator columns per tile
+constexpr int kBK = 64;           // K per stage (128 bytes of bf16: one swizzle row)
+constexpr int kStages = 4;
+constexpr int kLag = kStages - 1; // cp.async groups a producer keeps in flight
+constexpr int kABytes = kBM * kBK * 2;   // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;   // 32 KB
+constexpr int kEpiThreads = 128;
+constexpr int kProdThreads = 128;
+constexpr int kGemmThreads = kEpiThreads + kProdThreads + 32;
+constexpr int kTmemCols = 2 * kBN;
+constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 256;
+
+enum GemmMode { kGateUp = 0, kDown = 1 };
+
+struct GemmArgs {
+  const __nv_bfloat16* x;         // gate_up: [T, H] activations gathered by row
+  const int32_t* sorted_ids;      // [cap] pair index or sentinel num_pairs
+  const int32_t* expert_ids;      // [cap / 128]
+  const int32_t* ntpp;            // [1] padded rows in use
+  const float* topk_w;            // down: [num_pairs] route weights
+  __nv_bfloat16* h;               // gate_up out: [cap, I] in sorted order
+  float* y_acc;                   // down out: [T, H] fp32 accumulator
+  int* err;
+  int num_pairs, topk;
+  int K;                          // reduction length (H, or I)
+  int I, H;
+  int n_tiles;                    // n-blocks per m-block
+  int b_rows_per_expert;          // rows of the 2D weight view per expert (2I, or H)
+};
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                    const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sA = raw_addr + pad;                       // kStages x 16 KB
+  const uint32_t sB = sA + kStages * kABytes;               // kStages x 32 KB
+  uint8_t* ctl = smem + kStages * (kABytes + kBBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ctl);
+  // bars: full[kStages], empty[kStages], tfull[2], tempty[2], done
+  const uint32_t bar_base = ptx::smem_u32(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (kStages + s); };
+  auto tfull_bar = [&](int b) { return bar_base + 8u * (2 * kStages + b); };
+  auto tempty_bar = [&](int b) { return bar_base + 8u * (2 * kStages + 2 + b); };
+  const uint32_t done_bar = bar_base + 8u * (2 * kStages + 4);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 128);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 132);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(full_bar(s), MODE == kGateUp ? kProdThreads + 1 : 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(tfull_bar(b), 1);
+      ptx::mbar_init(tempty_bar(b), kEpiThreads);
+    }
+    ptx::mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 8) {
+    ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (tid == kEpiThreads) {
+    ptx::prefetch_tmap(&map_b);
+    if (MODE == kDown) ptx::prefetch_tmap(&map_a);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int m_tiles = __ldg(args.ntpp) / kBM;
+  const int tiles = m_tiles * args.n_tiles;
+  const int kblocks = args.K / kBK;
+
+  if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ producers
+    const int p = tid - kEpiThreads;
+    const bool leader = (p == 0);
+    int stage = 0;
+    uint32_t phase = 0;
+    int pending = 0;                  // gate_up: issued cp.async groups not yet arrived on
+    int fills[kStages] = {0, 0, 0, 0};  // leader: TMA fills issued per stage
+    const int chunk = p & 7;          // 16-byte chunk of the 128-byte row
+    const int rgrp = p >> 3;          // rows rgrp + 16 * i
+    bool ok = true;
+    if (MODE == kGateUp || leader) {
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int mt = t / args.n_tiles;
+        const int nt = t - mt * args.n_tiles;
+        const int e = __ldg(args.expert_ids + mt);
+        int tok[8];
+        if (MODE == kGateUp) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int sid = __ldg(args.sorted_ids + mt * kBM + rgrp + 16 * i);
+            tok[i] = (sid < args.num_pairs) ? sid / args.topk : -1;
+          }
+        }
+        const int b_row0 = e * args.b_rows_per_expert + nt * (MODE == kGateUp ? kBM : kBN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
+          const uint32_t a_dst = sA + stage * kABytes;
+          const uint32_t b_dst = sB + stage * kBBytes;
+          if (leader) {
+            const uint32_t bytes = kBBytes + (MODE == kDown ? kABytes : 0);
+            ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
+            if (MODE == kGateUp) {
+              ptx::tma_load_2d(b_dst, &map_b, full_bar(stage), kb * kBK, b_row0);
+              ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(stage), kb * kBK, b_row0 + args.I);
+            } else {
+              ptx::tma_load_2d(b_dst, &map_b, full_bar(stage), kb * kBK, b_row0);
+              ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(stage), kb * kBK, b_row0 + kBM);
+              ptx::tma_load_2d(a_dst, &map_a, full_bar(stage), kb * kBK, mt * kBM);
+            }
+            ++fills[stage];
+          }
+          if (MODE == kGateUp) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = rgrp + 16 * i;
+              const uint32_t dst = a_dst + r * 128 + ((chunk ^ (r & 7)) << 4);
+              const __nv_bfloat16* src =
+                  tok[i] >= 0 ? args.x + static_cast<size_t>(tok[i]) * args.K + kb * kBK + chunk * 8 : args.x;
+              ptx::cp_async_16(dst, src, tok[i] >= 0 ? 16u : 0u);
+            }
+            ptx::cp_async_commit();
+            if (++pending > kLag) {
+              // the oldest group (issued kLag stages ago) has landed: publish it to the async proxy
+              ptx::cp_async_wait<kLag>();
+              ptx::fence_proxy_async_smem();
+              ptx::mbar_arrive(full_bar((stage - kLag + kStages) % kStages));
+              --pending;
+            }
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+    if (MODE == kGateUp) {
+      ptx::cp_async_wait<0>();
+      ptx::fence_proxy_async_smem();
+      for (int i = pending; i > 0; --i) ptx::mbar_arrive(full_bar((stage - i + kStages) % kStages));
+    }
+    if (leader) {
+      // never leave with bulk copies still writing this CTA's shared memory
+#pragma unroll
+      for (int st = 0; st < kStages; ++st)
+        if (fills[st] > 0) ptx::mbar_wait_drain(full_bar(st), (fills[st] - 1) & 1);
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    if (ptx::elect_one()) {
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, kBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++it) {
+        const int b = it & 1;
+        const uint32_t tphase = (it >> 1) & 1;
+        if (!ptx::mbar_wait(tempty_bar(b), tphase ^ 1u, abort_flag)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + b * kBN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint64_t adesc = ptx::sdesc_sw128(sA + stage * kABytes);
+          const uint64_t bdesc = ptx::sdesc_sw128(sB + stage * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            ptx::mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          ptx::mma_commit(empty_bar(stage));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (ok) ptx::mma_commit(tfull_bar(b));
+      }
+      // all issued MMAs complete before TMEM is released
+      ptx::mma_commit(done_bar);
+      ptx::mbar_wait_drain(done_bar, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int r = warp * 32 + lane;  // accumulator row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    int it = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+      const int b = it & 1;
+      const uint32_t tphase = (it >> 1) & 1;
+      const int mt = t / args.n_tiles;
+      const int nt = t - mt * args.n_tiles;
+      const int pos = mt * kBM + r;
+      const int sid = __ldg(args.sorted_ids + pos);
+      if (!ptx::mbar_wait(tfull_bar(b), tphase, abort_flag)) break;
+      ptx::tc_fence_after();
+      const uint32_t tbase = tmem_base + lane_off + b * kBN;
+      if (MODE == kGateUp) {
+        const int n0 = nt * kBM;
+        __nv_bfloat16* hrow = args.h + static_cast<size_t>(pos) * args.I + n0;
+#pragma unroll 1
+        for (int c = 0; c < kBM / 32; ++c) {
+          uint32_t g[32], u[32];
+          ptx::tmem_ld32(tbase + c * 32, g);
+          ptx::tmem_ld32(tbase + kBM + c * 32, u);
+          ptx::tmem_ld_wait();
+          uint32_t packed[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+            const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
+            packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(hrow + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+        }
+      } else {
+        const bool valid = sid < args.num_pairs;
+        const float w = valid ? __ldg(args.topk_w + sid) : 0.f;
+        const int tok = valid ? sid / args.topk : 0;
+        float* yrow = args.y_acc + static_cast<size_t>(tok) * args.H + nt * kBN;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t d[32];
+          ptx::tmem_ld32(tbase + c * 32, d);
+          ptx::tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 v = make_float4(w * __uint_as_float(d[4 * q]), w * __uint_as_float(d[4 * q + 1]),
+                                           w * __uint_as_float(d[4 * q + 2]), w * __uint_as_float(d[4 * q + 3]));
+              atomicAdd(reinterpret_cast<float4*>(yrow + c * 32 + 4 * q), v);
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tempty_bar(b));
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 8) ptx::tmem_dealloc(tmem_base, kTmemCols);
+  if (tid == 0 && *abort_flag) report_error(args.err, MOE_DEVERR_TIMEOUT);
+}
+
+// ----------------------------------------------------------------------------- host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+// 2D bf16 tensor map over a row-major [rows, cols] matrix, box = 64 cols x 128 rows, 128B swizzle.
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+  auto encode = get_encode_fn();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+moe_status_t launch_gemm_gate_up(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_ids,
+                                 const int32_t* expert_ids, const int32_t* ntpp, __nv_bfloat16* h, int* err,
+                                 int num_pairs, int topk, int H, int I, int E, cudaStream_t s) {
+  CUtensorMap map_b;
+  if (!make_tmap_bf16_2d(&map_b, w1, static_cast<uint64_t>(E) * 2 * I, H)) return MOE_ERR_CUDA;
+  GemmArgs a{};
+  a.x = x; a.sorted_ids = sorted_ids; a.expert_ids = expert_ids; a.ntpp = ntpp; a.h = h; a.err = err;
+  a.num_pairs = num_pairs; a.topk = topk; a.K = H; a.I = I; a.H = H;
+  a.n_tiles = I / kBM; a.b_rows_per_expert = 2 * I;
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_gemm_kernel<kGateUp>), static_cast<int>(kGemmSmem)))
+    return MOE_ERR_CUDA;
+  moe_gemm_kernel<kGateUp><<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_b, map_b, a);
+  return launch_status();
+}
+
+moe_status_t launch_gemm_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, const int32_t* sorted_ids,
+                              const int32_t* expert_ids, const int32_t* ntpp, const float* topk_w, float* y_acc,
+                              int* err, int num_pairs, int topk, int cap, int H, int I, int E, cudaStream_t s) {
+  CUtensorMap map_a, map_b;
+  if (!make_tmap_bf16_2d(&map_a, h, static_cast<uint64_t>(cap), I)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d(&map_b, w2, static_cast<uint64_t>(E) * H, I)) return MOE_ERR_CUDA;
+  GemmArgs a{};
+  a.sorted_ids = sorted_ids; a.expert_ids = expert_ids; a.ntpp = ntpp; a.topk_w = topk_w; a.y_acc = y_acc;
+  a.err = err; a.num_pairs = num_pairs; a.topk = topk; a.K = I; a.I = I; a.H = H;
+  a.n_tiles = H / kBN; a.b_rows_per_expert = H;
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_gemm_kernel<kDown>), static_cast<int>(kGemmSmem)))
+    return MOE_ERR_CUDA;
+  moe_gemm_kernel<kDown><<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_a, map_b, a);
+  return launch_status();
+}
+
+}  // namespace moe

@@ -1,0 +1,31 @@
+"""Helpers shared by the GPU parity tests (comparison rules; no method arithmetic)."""
+import numpy as np
+import pytest
+import torch
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from mixture_experts_routing_grouped_gb300 import build
+    build.build()
+
+
+def assert_weights_close(got, ref, rel=1e-6):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    bad = np.abs(got - ref) > rel * np.abs(ref)
+    assert not bad.any(), f"{bad.sum()} weights off by more than {rel} relative; worst {np.abs(got-ref).max()}"
+
+
+def assert_moe_close(got, ref):
+    """bf16 layer output vs the float64 oracle: |d| <= 2e-2 * max(1, |ref|) per element,
+    and relative Frobenius error <= 1e-2."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    d = np.abs(got - ref)
+    bound = 2e-2 * np.maximum(1.0, np.abs(ref))
+    assert (d <= bound).all(), f"max |dy| = {d.max():.3e} at {np.unravel_index(d.argmax(), d.shape)}"
+    nref = np.linalg.norm(ref)
+    if nref > 0:
+        assert np.linalg.norm(got - ref) <= 1e-2 * nref, f"rel fro {np.linalg.norm(got - ref) / nref:.3e}"

@@ -1,0 +1,90 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+validation and size queries behave as documented. No GPU needed: nothing here
+launches a kernel."""
+import ctypes
+import pathlib
+import re
+
+import pytest
+
+from conftest import ROOT
+from oracle import align as oalign
+
+HEADER = ROOT / "include" / "moe_gb300.h"
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mixture_experts_routing_grouped_gb300 import build
+    build.build()
+    import mixture_experts_routing_grouped_gb300 as moe
+    return moe.lib()
+
+
+def _declared():
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"^MOE_API [^(]*?\b(\w+)\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ["moe_grouped_topk", "moe_align_block_size", "moe_align_max_padded", "moe_fused_forward",
+              "moe_fused_forward_workspace_size", "gmm_lowp", "moe_quant_per_token", "moe_check_device_error",
+              "moe_status_string"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    import mixture_experts_routing_grouped_gb300 as moe
+    for n in _declared():
+        assert hasattr(L, n), n
+    assert sorted(moe.exported_symbols()) == _declared()
+
+
+def test_status_strings(L):
+    assert L.moe_status_string(0) == b"MOE_OK"
+    assert L.moe_status_string(3) == b"MOE_ERR_WORKSPACE"
+    assert L.moe_status_string(99) == b"MOE_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("n,E,bm", [(0, 8, 4), (10, 8, 4), (32768, 128, 128), (1024, 256, 16), (5, 1000, 256)])
+def test_align_capacity_matches_oracle(L, n, E, bm):
+    assert L.moe_align_max_padded(n, E, bm) == oalign.max_padded(n, E, bm)
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: validation returns before any launch
+
+
+def test_routing_validation(L):
+    f = L.moe_grouped_topk
+    assert f(FAKE, 4, 10, 3, 1, 1, 0, 1, 1.0, FAKE, FAKE, None) == 1      # E % G != 0
+    assert f(FAKE, 4, 8, 4, 5, 1, 0, 1, 1.0, FAKE, FAKE, None) == 1       # topk_group > G
+    assert f(FAKE, 4, 8, 4, 2, 5, 0, 1, 1.0, FAKE, FAKE, None) == 1       # topk > candidates
+    assert f(FAKE, 4, 2048, 8, 4, 8, 0, 1, 1.0, FAKE, FAKE, None) == 1    # E > 1024
+    assert f(FAKE, 4, 8, 1, 1, 2, 7, 1, 1.0, FAKE, FAKE, None) == 1       # unknown scoring
+    assert f(None, 4, 8, 1, 1, 2, 0, 1, 1.0, FAKE, FAKE, None) == 1       # null input
+    assert f(ctypes.c_void_p(0x10004), 4, 8, 1, 1, 2, 0, 1, 1.0, FAKE, FAKE, None) == 2  # misaligned
+    assert f(None, 0, 8, 1, 1, 2, 0, 1, 1.0, None, None, None) == 0       # T = 0: nothing to do
+
+
+def test_align_validation(L):
+    f = L.moe_align_block_size
+    assert f(FAKE, 10, 8, 3, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, None) == 1  # block_m not a power of 2
+    assert f(FAKE, 10, 8, 512, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, None) == 1
+    assert f(FAKE, 10, 0, 4, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, None) == 1
+    assert f(FAKE, 10, 8, 4, FAKE, FAKE, FAKE, FAKE, None, 4096, None) == 3   # no workspace
+    assert f(FAKE, 10, 8, 4, FAKE, FAKE, FAKE, FAKE, FAKE, 8, None) == 3      # workspace too small
+
+
+def test_fused_validation_and_sizes(L):
+    f = L.moe_fused_forward
+    ws = L.moe_fused_forward_workspace_size(4096, 2048, 768, 128, 8)
+    cap = oalign.max_padded(4096 * 8, 128, 128)
+    assert ws >= cap * 768 * 2 + 4096 * 2048 * 4
+    args = lambda H, I, wsb, wsp=FAKE: (FAKE, FAKE, FAKE, FAKE, 64, H, I, 8, 1, 1, 2, 0, 1, 1.0, FAKE, FAKE, FAKE,
+                                        wsp, wsb, None)
+    assert f(*args(100, 256, 1 << 30)) == 2          # H not a multiple of 256
+    assert f(*args(512, 200, 1 << 30)) == 2          # I not a multiple of 128
+    need = L.moe_fused_forward_workspace_size(64, 512, 256, 8, 2)
+    assert f(*args(512, 256, need - 1)) == 3
+    assert f(*args(512, 256, need, ctypes.c_void_p(0x10010))) == 3  # workspace not 256-byte aligned
