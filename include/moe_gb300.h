@@ -145,6 +145,36 @@ MOE_API moe_status_t moe_fused_forward(const void* x, const float* gating, const
                                size_t ws_bytes, void* stream);
 
 /*
+ * moe_fused_forward_noalloc -- moe_fused_forward without a caller-provided workspace.
+ * The pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory (a plug-in or backend inside a host framework that owns
+ * all device memory and hands out no workspace; a latency-critical caller that
+ * cannot afford cudaMalloc, which may synchronise the device).
+ *
+ * Arguments, outputs and results are those of moe_fused_forward; the scratch comes
+ * from a fixed MOE_NOALLOC_SCRATCH_BYTES array inside the library, which every GPU
+ * that loads the library's device code holds until the process exits. The call
+ * allocates nothing.
+ *  - Problems whose moe_fused_forward_workspace_size(T, H, I, E, topk) exceeds
+ *    MOE_NOALLOC_SCRATCH_BYTES are rejected with MOE_ERR_WORKSPACE, before any launch.
+ *  - The first call made while a device is current looks up the array's device
+ *    address on that device (cudaGetSymbolAddress) and caches it; make that first
+ *    call before any stream capture on the device.
+ *  - All calls share the array, which keeps the last call's contents (nothing in
+ *    it needs to start at zero). Calls whose GPU work overlaps (different streams
+ *    or host threads) race on it: serialise them.
+ *  - The device error word of this scratch is not exposed.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+MOE_API moe_status_t moe_fused_forward_noalloc(const void* x, const float* gating,
+                                               const void* w_gate_up, const void* w_down, int T,
+                                               int H, int I, int E, int num_expert_group,
+                                               int topk_group, int topk, int scoring,
+                                               int renormalize, float routed_scaling_factor,
+                                               void* y, float* topk_weights, int32_t* topk_ids,
+                                               void* stream);
+
+/*
  * moe_set_stage_events -- optional per-stage timing of moe_fused_forward (not in the
  * pages; instrumentation only). While set, every moe_fused_forward call made by
  * the calling host thread records events[0] on its stream before the routing

@@ -30,6 +30,8 @@ _SIGNATURES = {
     "moe_fused_forward_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "moe_fused_forward": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                    _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp, _c_size, _vp]),
+    "moe_fused_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                           _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp]),
     "moe_quant_per_token": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "gmm_lowp_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "gmm_lowp": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
@@ -171,6 +173,37 @@ def moe_fused_forward(x: torch.Tensor, gating: torch.Tensor, w_gate_up: torch.Te
                                  float(routed_scaling_factor), _ptr(y), _ptr(topk_weights), _ptr(topk_ids),
                                  _ptr(ws), ws.numel(), _stream(x))
     _check("moe_fused_forward", st)
+    return y, topk_weights, topk_ids
+
+
+def moe_fused_forward_noalloc(x: torch.Tensor, gating: torch.Tensor, w_gate_up: torch.Tensor, w_down: torch.Tensor,
+                              topk: int, renormalize: bool = True, num_expert_group: int = 1, topk_group: int = 1,
+                              scoring_func: str = "softmax", routed_scaling_factor: float = 1.0,
+                              y: torch.Tensor | None = None, topk_weights: torch.Tensor | None = None,
+                              topk_ids: torch.Tensor | None = None):
+    """moe_fused_forward with its scratch taken from the library's fixed device array instead
+    of a workspace: for callers that cannot allocate device memory. Outputs may be passed
+    in preallocated; problems needing more than MOE_NOALLOC_SCRATCH_BYTES of scratch raise
+    MoeError(MOE_ERR_WORKSPACE). Calls that overlap on the GPU race on the shared array."""
+    _need(x, "x", torch.bfloat16)
+    T, H = x.shape
+    E, I2, _ = w_gate_up.shape
+    I = I2 // 2
+    _need(gating, "gating", torch.float32, (T, E))
+    _need(w_gate_up, "w_gate_up", torch.bfloat16, (E, 2 * I, H))
+    _need(w_down, "w_down", torch.bfloat16, (E, H, I))
+    dev = x.device
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty((T, topk), dtype=torch.float32, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    st = lib().moe_fused_forward_noalloc(_ptr(x), _ptr(gating), _ptr(w_gate_up), _ptr(w_down), T, H, I, E,
+                                         num_expert_group, topk_group, topk, SCORING[scoring_func],
+                                         int(bool(renormalize)), float(routed_scaling_factor), _ptr(y),
+                                         _ptr(topk_weights), _ptr(topk_ids), _stream(x))
+    _check("moe_fused_forward_noalloc", st)
     return y, topk_weights, topk_ids
 
 
