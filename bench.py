@@ -276,6 +276,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
     if not args.skip_extra and world == 1:
         result["decode"] = bench_decode(moe, synth, torch, dev, flush, peaks, args)
         result["routing"] = bench_routing(moe, synth, torch, dev, flush, peaks, args)
+        result["gmm_lowp"] = bench_lowp(moe, synth, torch, dev, flush, peaks, args)
     del W
     return result, cfg
 
@@ -343,6 +344,47 @@ def bench_routing(moe, synth, torch, dev, flush, peaks, args):
         gbs = nbytes / (us * 1e-6) / 1e9
         out[f"T{T}"] = {"us": round(us, 2), "bytes": nbytes, "GB/s": round(gbs, 1),
                         "frac_hbm": round(gbs / float(peaks["hbm_gbs"]), 4)}
+    return out
+
+
+def bench_lowp(moe, synth, torch, dev, flush, peaks, args):
+    """Low-precision grouped GEMM, M=2048, K=N=4096, E=32 Zipf groups, bf16 out, INT8 and FP8-e4m3."""
+    cfg = synth.lowp_config()
+    d = synth.gmm_inputs(cfg, dev)
+    out = {}
+    sizes = d["expert_sizes"].cpu().tolist()
+    n_active = sum(1 for s_ in sizes if s_ > 0)
+    flops = 2.0 * cfg.M * cfg.N * cfg.K
+    for name, qdt in (("int8", torch.int8), ("e4m3", torch.float8_e4m3fn)):
+        qx, sx = moe.moe_quant_per_token(d["x"], qdt)
+        qw, sw = moe.moe_quant_per_token(d["w"].view(cfg.E * cfg.N, cfg.K), qdt)
+        qw = qw.view(cfg.E, cfg.N, cfg.K)
+        sw = sw.view(cfg.E, cfg.N)
+        y = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+        run = lambda: moe.gmm_lowp(qx, qw, sx, sw, d["expert_offsets"], d["expert_sizes"], torch.bfloat16, y, ws)
+        for _ in range(3):
+            run()
+        times = []
+        for k in range(max(10, args.steps)):
+            flush.fill_(float(k))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            run()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        if moe.moe_check_device_error(ws):
+            raise RuntimeError("gmm_lowp reported a device error")
+        ms = statistics.mean(times)
+        nbytes = n_active * cfg.N * cfg.K + cfg.M * cfg.K + cfg.M * cfg.N * 2 + cfg.M * 4 + cfg.E * cfg.N * 4
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        tf = flops / (ms * 1e-3) / 1e12
+        out[name] = {"us": round(ms * 1e3, 2), "TFLOP/s": round(tf, 1),
+                     "frac_bf16_peak": round(tf / float(peaks["bf16_tflops"]), 4), "GB/s": round(gbs, 1),
+                     "frac_hbm": round(gbs / float(peaks["hbm_gbs"]), 4), "bytes": nbytes}
+    del d
+    torch.cuda.empty_cache()
     return out
 
 

@@ -7,13 +7,14 @@
 // padding, the expert of every block.
 //
 // One CTA of 1024 threads. Warp w owns the contiguous pair range
-// [w*S, (w+1)*S); walking it 32 pairs at a time, __match_any_sync groups the
-// lanes that carry the same expert, so a pair's rank among the equal experts
-// of one step is the popcount of its lower peers. Pass 1 counts per (warp,
-// expert) into shared memory, a block scan over experts turns the counts into
-// per-(warp, expert) write cursors, pass 2 re-walks the range and writes each
-// pair at cursor + in-step rank. Walking ranges in order makes the sort stable;
-// no atomics decide positions.
+// [w*S, (w+1)*S). Pass 1 counts the warp's pairs per expert into its own row of
+// a shared [warp][expert] table (shared-memory atomics; counts do not depend on
+// order). A block scan over experts turns the table into per-(warp, expert)
+// write cursors. Pass 2 re-walks the range in order, 32 pairs at a time:
+// __match_any_sync groups the lanes that carry the same expert, a pair's rank
+// among them is the popcount of its lower peers, and it lands at cursor + rank.
+// Walking the ranges in order makes the sort stable; no atomics decide
+// positions. Ids are loaded kUnroll steps ahead so the loads overlap.
 #include "common.cuh"
 
 #include <algorithm>
@@ -23,6 +24,7 @@ namespace {
 
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
+constexpr int kUnroll = 8;  // ids per lane loaded before they are used
 
 __global__ void __launch_bounds__(kAlignThreads, 1)
     align_kernel(const int32_t* __restrict__ ids, int num_pairs, int E, int block_m, int cap,
@@ -45,17 +47,22 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   const int lo = min(num_pairs, warp * span);
   const int hi = min(num_pairs, lo + span);
 
-  // Pass 1: per-(warp, expert) counts.
-  for (int b = lo; b < hi; b += 32) {
-    const int p = b + lane;
-    int e = -1;
-    if (p < hi) {
-      e = ids[p];
-      if (e < 0 || e >= E) { report_error(err, MOE_DEVERR_EXPERT_ID); e = -1; }
+  // Pass 1: per-(warp, expert) counts; kUnroll ids per lane in flight.
+  for (int b = lo; b < hi; b += 32 * kUnroll) {
+    int e[kUnroll];
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int p = b + j * 32 + lane;
+      e[j] = (p < hi) ? __ldg(ids + p) : -1;
     }
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && (peers & lt_mask) == 0) cur[warp * E + e] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int p = b + j * 32 + lane;
+      if (p < hi) {
+        if (e[j] < 0 || e[j] >= E) report_error(err, MOE_DEVERR_EXPERT_ID);
+        else atomicAdd(&cur[warp * E + e[j]], 1);
+      }
+    }
   }
   __syncthreads();
 
@@ -105,23 +112,28 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   for (int blk = total / block_m + tid; blk < cap / block_m; blk += kAlignThreads) expert_ids[blk] = -1;
   __syncthreads();
 
-  // Pass 2: stable placement.
-  for (int b = lo; b < hi; b += 32) {
-    const int p = b + lane;
-    int e = -1;
-    if (p < hi) {
-      e = ids[p];
-      if (e < 0 || e >= E) e = -1;
+  // Pass 2: stable placement, walking the warp's range in order.
+  for (int b = lo; b < hi; b += 32 * kUnroll) {
+    int e[kUnroll];
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int p = b + j * 32 + lane;
+      const int v = (p < hi) ? __ldg(ids + p) : -1;
+      e[j] = (v >= 0 && v < E) ? v : -1;
     }
-    const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    int base = 0;
-    if (e >= 0) base = cur[warp * E + e];
-    __syncwarp();
-    if (e >= 0) {
-      sorted_ids[base + __popc(peers & lt_mask)] = p;
-      if ((peers & lt_mask) == 0) cur[warp * E + e] = base + __popc(peers);
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int p = b + j * 32 + lane;
+      const uint32_t peers = __match_any_sync(0xffffffffu, e[j]);
+      int base = 0;
+      if (e[j] >= 0) base = cur[warp * E + e[j]];
+      __syncwarp();
+      if (e[j] >= 0) {
+        sorted_ids[base + __popc(peers & lt_mask)] = p;
+        if ((peers & lt_mask) == 0) cur[warp * E + e[j]] = base + __popc(peers);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   }
 }
 

@@ -107,7 +107,8 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   if (!aligned16(x) || !aligned16(gating) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y))
     return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
-  if (static_cast<long long>(T) * topk >= (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(T) * topk >= (1ll << 30) || static_cast<long long>(T) * H >= (1ll << 31))
+    return MOE_ERR_UNSUPPORTED;
   const FusedLayout L = fused_layout(T, H, I, E, topk);
   if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
   if (T == 0) return MOE_OK;

@@ -16,8 +16,10 @@
 //
 // Kernel shape (one persistent CTA per SM, 288 threads):
 //   warps 0-3  epilogue: TMEM -> registers -> global (TMEM lane quarter = warp)
-//   warps 4-7  producers: cp.async gather of A rows (gate_up pass), TMA for B
-//              (and for A in the down pass), 4-stage shared-memory ring
+//   warps 4-7  producers. gate_up: warp w owns ring slot w and stages every
+//              4th k-block (TMA for B, cp.async row gather for A), so four
+//              stages are in flight without any warp waiting on another's copies.
+//              down: one thread sends A and B by TMA through the 4-stage ring.
 //   warp 8     TMEM allocation and the single MMA-issuing thread
 // The 128 x 256 fp32 accumulator lives in TMEM, double-buffered (512 columns)
 // so that the epilogue of one tile overlaps the main loop of the next.
@@ -36,14 +38,14 @@ constexpr int kBM = 128;          // rows per tile (= align block_m)
 constexpr int kBN = 256;          // accumulator columns per tile
 constexpr int kBK = 64;           // K per stage (128 bytes of bf16: one swizzle row)
 constexpr int kStages = 4;
-constexpr int kLag = kStages - 1; // cp.async groups a producer keeps in flight
 constexpr int kABytes = kBM * kBK * 2;   // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;   // 32 KB
 constexpr int kEpiThreads = 128;
 constexpr int kProdThreads = 128;
 constexpr int kGemmThreads = kEpiThreads + kProdThreads + 32;
 constexpr int kTmemCols = 2 * kBN;
-constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 256;
+constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 256 + 4 * kBM * 4;
+static_assert(kStages == 4, "one producer warp per ring slot");
 
 enum GemmMode { kGateUp = 0, kDown = 1 };
 
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(full_bar(s), MODE == kGateUp ? kProdThreads + 1 : 1);
+      ptx::mbar_init(full_bar(s), MODE == kGateUp ? 32 + 1 : 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -123,75 +125,84 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ producers
-    const int p = tid - kEpiThreads;
-    const bool leader = (p == 0);
-    int stage = 0;
-    uint32_t phase = 0;
-    int pending = 0;                  // gate_up: issued cp.async groups not yet arrived on
-    int fills[kStages] = {0, 0, 0, 0};  // leader: TMA fills issued per stage
-    const int chunk = p & 7;          // 16-byte chunk of the 128-byte row
-    const int rgrp = p >> 3;          // rows rgrp + 16 * i
-    bool ok = true;
-    if (MODE == kGateUp || leader) {
+    const int pw = warp - 4;
+    if (MODE == kGateUp) {
+      // Producer warp pw owns ring slot pw (kStages == 4 == producer warps) and
+      // stages every 4th k-block of this CTA's (tile, k-block) sequence: lane 0
+      // sends the B tile by TMA, the 32 lanes gather the 128 A rows with cp.async
+      // (16 B each, zero-fill for pad rows) into the 128B-swizzled layout, wait
+      // for their own copies, publish them to the async proxy and arrive.
+      int* rowtab = reinterpret_cast<int*>(ctl + 256) + pw * kBM;  // element offset of each row, -1 = pad
+      int cached_t = -1, e = 0, fills = 0;
+      const int slot = pw;
+      const uint32_t a_dst = sA + slot * kABytes;
+      const uint32_t b_dst = sB + slot * kBBytes;
+      const int chunk = lane & 7;
+      const int rsub = lane >> 3;
+      for (int g = pw;; g += kStages) {
+        const int t_local = g / kblocks;
+        const int t = blockIdx.x + t_local * gridDim.x;
+        if (t >= tiles) break;
+        const int kb = g - t_local * kblocks;
+        const int mt = t / args.n_tiles;
+        const int nt = t - mt * args.n_tiles;
+        if (t != cached_t) {
+#pragma unroll
+          for (int q = 0; q < kBM / 32; ++q) {
+            const int sid = __ldg(args.sorted_ids + mt * kBM + q * 32 + lane);
+            rowtab[q * 32 + lane] = (sid < args.num_pairs) ? (sid / args.topk) * args.K : -1;
+          }
+          e = __ldg(args.expert_ids + mt);
+          cached_t = t;
+          __syncwarp();
+        }
+        const uint32_t use = static_cast<uint32_t>(g / kStages);
+        if (!ptx::mbar_wait(empty_bar(slot), (use & 1u) ^ 1u, abort_flag)) break;
+        if (lane == 0) {
+          const int b_row0 = e * args.b_rows_per_expert + nt * kBM;
+          ptx::mbar_arrive_expect_tx(full_bar(slot), kBBytes);
+          ptx::tma_load_2d(b_dst, &map_b, full_bar(slot), kb * kBK, b_row0);
+          ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(slot), kb * kBK, b_row0 + args.I);
+          ++fills;
+        }
+        const int k0 = kb * kBK + chunk * 8;
+#pragma unroll 8
+        for (int i = 0; i < kBM / 4; ++i) {
+          const int r = i * 4 + rsub;
+          const int off = rowtab[r];
+          const uint32_t dst = a_dst + r * 128 + ((chunk ^ (r & 7)) << 4);
+          ptx::cp_async_16(dst, off >= 0 ? args.x + off + k0 : args.x, off >= 0 ? 16u : 0u);
+        }
+        ptx::cp_async_commit();
+        ptx::cp_async_wait<0>();
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(full_bar(slot));
+      }
+      ptx::cp_async_wait<0>();
+      // never leave with bulk copies still writing this CTA's shared memory
+      if (lane == 0 && fills > 0) ptx::mbar_wait_drain(full_bar(slot), (fills - 1) & 1);
+    } else if (tid == kEpiThreads) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int fills[kStages] = {0, 0, 0, 0};
+      bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         const int mt = t / args.n_tiles;
         const int nt = t - mt * args.n_tiles;
         const int e = __ldg(args.expert_ids + mt);
-        int tok[8];
-        if (MODE == kGateUp) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int sid = __ldg(args.sorted_ids + mt * kBM + rgrp + 16 * i);
-            tok[i] = (sid < args.num_pairs) ? sid / args.topk : -1;
-          }
-        }
-        const int b_row0 = e * args.b_rows_per_expert + nt * (MODE == kGateUp ? kBM : kBN);
+        const int b_row0 = e * args.b_rows_per_expert + nt * kBN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t a_dst = sA + stage * kABytes;
           const uint32_t b_dst = sB + stage * kBBytes;
-          if (leader) {
-            const uint32_t bytes = kBBytes + (MODE == kDown ? kABytes : 0);
-            ptx::mbar_arrive_expect_tx(full_bar(stage), bytes);
-            if (MODE == kGateUp) {
-              ptx::tma_load_2d(b_dst, &map_b, full_bar(stage), kb * kBK, b_row0);
-              ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(stage), kb * kBK, b_row0 + args.I);
-            } else {
-              ptx::tma_load_2d(b_dst, &map_b, full_bar(stage), kb * kBK, b_row0);
-              ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(stage), kb * kBK, b_row0 + kBM);
-              ptx::tma_load_2d(a_dst, &map_a, full_bar(stage), kb * kBK, mt * kBM);
-            }
-            ++fills[stage];
-          }
-          if (MODE == kGateUp) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int r = rgrp + 16 * i;
-              const uint32_t dst = a_dst + r * 128 + ((chunk ^ (r & 7)) << 4);
-              const __nv_bfloat16* src =
-                  tok[i] >= 0 ? args.x + static_cast<size_t>(tok[i]) * args.K + kb * kBK + chunk * 8 : args.x;
-              ptx::cp_async_16(dst, src, tok[i] >= 0 ? 16u : 0u);
-            }
-            ptx::cp_async_commit();
-            if (++pending > kLag) {
-              // the oldest group (issued kLag stages ago) has landed: publish it to the async proxy
-              ptx::cp_async_wait<kLag>();
-              ptx::fence_proxy_async_smem();
-              ptx::mbar_arrive(full_bar((stage - kLag + kStages) % kStages));
-              --pending;
-            }
-          }
+          ptx::mbar_arrive_expect_tx(full_bar(stage), kBBytes + kABytes);
+          ptx::tma_load_2d(b_dst, &map_b, full_bar(stage), kb * kBK, b_row0);
+          ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(stage), kb * kBK, b_row0 + kBM);
+          ptx::tma_load_2d(a_dst, &map_a, full_bar(stage), kb * kBK, mt * kBM);
+          ++fills[stage];
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
-    }
-    if (MODE == kGateUp) {
-      ptx::cp_async_wait<0>();
-      ptx::fence_proxy_async_smem();
-      for (int i = pending; i > 0; --i) ptx::mbar_arrive(full_bar((stage - i + kStages) % kStages));
-    }
-    if (leader) {
-      // never leave with bulk copies still writing this CTA's shared memory
 #pragma unroll
       for (int st = 0; st < kStages; ++st)
         if (fills[st] > 0) ptx::mbar_wait_drain(full_bar(st), (fills[st] - 1) & 1);
@@ -326,6 +337,22 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 2D 8-bit tensor map over a row-major [rows, cols] byte matrix, box = 128 x 128,
+// 128B swizzle (tcgen05 operand) or none (staging read back by threads).
+bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, bool swizzle128) {
+  auto encode = get_encode_fn();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
