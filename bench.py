@@ -441,6 +441,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-extra", action="store_true", help="skip the decode and routing sub-benchmarks")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["routing", "decode", "lowp"],
+                    help="run just one sub-benchmark on one GPU and print its JSON (profiling cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local_rank = dist_env()
@@ -449,6 +451,19 @@ def main():
         if rank != 0:
             return
         print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+
+    if args.only:
+        import torch
+        import mixture_experts_routing_grouped_gb300 as moe
+        import synth
+        from mixture_experts_routing_grouped_gb300 import build as _b
+        _b.build()
+        peaks, _ = load_peaks()
+        dev = torch.device("cuda", local_rank)
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        fn = {"routing": bench_routing, "decode": bench_decode, "lowp": bench_lowp}[args.only]
+        print(json.dumps({args.only: fn(moe, synth, torch, dev, flush, peaks, args)}), flush=True)
         return
 
     if world > 1:

@@ -103,9 +103,11 @@ MOE_API moe_status_t moe_grouped_topk(const float* gating, int T, int E, int num
  *  expert_offsets    [E + 1] int32 out: start of every expert's padded segment, then
  *                    the total.
  *  num_tokens_post_padded  [1] int32 out: the total padded length.
- *  ws, ws_bytes      workspace of at least moe_align_workspace_size(...) bytes
- *                    (its first 4 bytes are the device error word; ids outside
- *                    [0, E) are skipped and set MOE_DEVERR_EXPERT_ID).
+ *  ws, ws_bytes      workspace of at least moe_align_workspace_size(...) bytes,
+ *                    256-byte aligned and zero-filled before its first use (the
+ *                    call keeps a completion ticket there and leaves it at zero).
+ *                    Its first 4 bytes are the device error word; ids outside
+ *                    [0, E) are skipped and set MOE_DEVERR_EXPERT_ID.
  */
 MOE_API size_t moe_align_max_padded(int num_pairs, int E, int block_m);
 MOE_API size_t moe_align_workspace_size(int num_pairs, int E, int block_m);
@@ -133,7 +135,8 @@ MOE_API moe_status_t moe_align_block_size(const int32_t* topk_ids, int num_pairs
  *  y            [T, H] bf16 out: sum_j w[t,j] * W2[e] (silu(G_e x_t) * U_e x_t).
  *  topk_weights [T, topk] fp32 out, topk_ids [T, topk] int32 out (the routing).
  *  ws, ws_bytes workspace of at least moe_fused_forward_workspace_size(...) bytes,
- *               256-byte aligned; holds the sorted pair layout, h = silu(gate)*up in sorted order and
+ *               256-byte aligned and zero-filled before its first use (a ticket
+ *               counter inside is left at zero by every call); holds the sorted pair layout, h = silu(gate)*up in sorted order and
  *               an fp32 accumulator for y. Its first 4 bytes are the device error word.
  */
 MOE_API size_t moe_fused_forward_workspace_size(int T, int H, int I, int E, int topk);

@@ -6,15 +6,19 @@
 // every pair at seg_start[e] + rank-within-expert, sentinel num_pairs in the
 // padding, the expert of every block.
 //
-// One CTA of 1024 threads. Warp w owns the contiguous pair range
-// [w*S, (w+1)*S). Pass 1 counts the warp's pairs per expert into its own row of
-// a shared [warp][expert] table (shared-memory atomics; counts do not depend on
-// order). A block scan over experts turns the table into per-(warp, expert)
-// write cursors. Pass 2 re-walks the range in order, 32 pairs at a time:
-// __match_any_sync groups the lanes that carry the same expert, a pair's rank
-// among them is the popcount of its lower peers, and it lands at cursor + rank.
-// Walking the ranges in order makes the sort stable; no atomics decide
-// positions. Ids are loaded kUnroll steps ahead so the loads overlap.
+// Two kernels over chunks of S consecutive pairs (one CTA per chunk):
+//  1. count: per-chunk expert histogram (shared-memory atomics; counts do not
+//     depend on order) written to the workspace; the last CTA to finish (a
+//     ticket taken after a fence) scans the histograms: per-expert totals,
+//     padded lengths, segment starts, and for every chunk the position where its
+//     first pair of each expert lands. It also writes offsets, the padded
+//     length, the block experts and the sentinels.
+//  2. scatter: each chunk is re-read in order. Warp w owns a contiguous slice;
+//     a shared [warp][expert] table gives each warp's write cursors; walking its
+//     slice 32 pairs at a time, __match_any_sync groups lanes with the same
+//     expert and a pair's rank among them is the popcount of its lower peers.
+// Walking every range in order makes the sort stable; no atomics decide
+// positions.
 #include "common.cuh"
 
 #include <algorithm>
@@ -24,52 +28,52 @@ namespace {
 
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
-constexpr int kUnroll = 8;  // ids per lane loaded before they are used
+constexpr int kMaxChunks = 512;
 
-__global__ void __launch_bounds__(kAlignThreads, 1)
-    align_kernel(const int32_t* __restrict__ ids, int num_pairs, int E, int block_m, int cap,
-                 int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
-                 int32_t* __restrict__ expert_offsets, int32_t* __restrict__ ntpp, int* __restrict__ err) {
-  extern __shared__ int smem[];
-  int* cur = smem;  // [kAlignWarps][E]: counts, then write cursors
+struct AlignPlan {
+  int chunk;    // pairs per chunk (multiple of 1024)
+  int nchunks;
+};
+
+AlignPlan align_plan(int num_pairs) {
+  AlignPlan p;
+  const int per = std::max(1, (num_pairs + kMaxChunks * 1024 - 1) / (kMaxChunks * 1024));
+  p.chunk = 1024 * per;
+  p.nchunks = std::max(1, (num_pairs + p.chunk - 1) / p.chunk);
+  return p;
+}
+
+__global__ void __launch_bounds__(kAlignThreads)
+    align_count_scan_kernel(const int32_t* __restrict__ ids, int num_pairs, int E, int block_m, int cap, int chunk,
+                            int nchunks, int32_t* __restrict__ chunk_base, int* __restrict__ done,
+                            int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+                            int32_t* __restrict__ expert_offsets, int32_t* __restrict__ ntpp, int* __restrict__ err) {
+  __shared__ int hist[MOE_MAX_EXPERTS];
   __shared__ int warp_tot[kAlignWarps];
-  __shared__ int total_s;
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const uint32_t lt_mask = (1u << lane) - 1u;
-
-  for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) cur[i] = 0;
+  __shared__ int is_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += kAlignThreads) hist[e] = 0;
   __syncthreads();
-
-  const int span = cdiv(num_pairs, kAlignWarps);
-  const int lo = min(num_pairs, warp * span);
-  const int hi = min(num_pairs, lo + span);
-
-  // Pass 1: per-(warp, expert) counts; kUnroll ids per lane in flight.
-  for (int b = lo; b < hi; b += 32 * kUnroll) {
-    int e[kUnroll];
-#pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const int p = b + j * 32 + lane;
-      e[j] = (p < hi) ? __ldg(ids + p) : -1;
-    }
-#pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const int p = b + j * 32 + lane;
-      if (p < hi) {
-        if (e[j] < 0 || e[j] >= E) report_error(err, MOE_DEVERR_EXPERT_ID);
-        else atomicAdd(&cur[warp * E + e[j]], 1);
-      }
-    }
+  const int lo = blockIdx.x * chunk;
+  const int hi = min(num_pairs, lo + chunk);
+  for (int p = lo + tid; p < hi; p += kAlignThreads) {
+    const int e = __ldg(ids + p);
+    if (e < 0 || e >= E) report_error(err, MOE_DEVERR_EXPERT_ID);
+    else atomicAdd(&hist[e], 1);
   }
   __syncthreads();
+  for (int e = tid; e < E; e += kAlignThreads) chunk_base[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = (atomicAdd(done, 1) == nchunks - 1);
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
 
-  // Scan over experts (one expert per thread; E <= 1024).
+  // Last CTA: totals, padded segments, per-chunk bases. One expert per thread (E <= 1024).
   int count = 0, padded = 0;
   if (tid < E) {
-    for (int w = 0; w < kAlignWarps; ++w) count += cur[w * E + tid];
+    for (int c = 0; c < nchunks; ++c) count += __ldcg(chunk_base + static_cast<size_t>(c) * E + tid);
     padded = (count + block_m - 1) / block_m * block_m;
   }
   int incl = padded;
@@ -87,19 +91,19 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
       const int n = __shfl_up_sync(0xffffffffu, t, o);
       if (lane >= o) t += n;
     }
-    warp_tot[lane] = t;  // inclusive prefix over warps
-    if (lane == 31) total_s = t;
+    warp_tot[lane] = t;
   }
   __syncthreads();
   const int start = incl - padded + (warp > 0 ? warp_tot[warp - 1] : 0);
-  const int total = total_s;
+  const int total = warp_tot[kAlignWarps - 1];
   if (tid < E) {
     expert_offsets[tid] = start;
-    int c = start;
-    for (int w = 0; w < kAlignWarps; ++w) {  // counts -> cursors
-      const int n = cur[w * E + tid];
-      cur[w * E + tid] = c;
-      c += n;
+    int run = start;
+    for (int c = 0; c < nchunks; ++c) {
+      int32_t* slot = chunk_base + static_cast<size_t>(c) * E + tid;
+      const int n = __ldcg(slot);
+      *slot = run;
+      run += n;
     }
     for (int blk = start / block_m; blk < (start + padded) / block_m; ++blk) expert_ids[blk] = tid;
     for (int pos = start + count; pos < start + padded; ++pos) sorted_ids[pos] = num_pairs;
@@ -110,30 +114,51 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   }
   for (int pos = total + tid; pos < cap; pos += kAlignThreads) sorted_ids[pos] = num_pairs;
   for (int blk = total / block_m + tid; blk < cap / block_m; blk += kAlignThreads) expert_ids[blk] = -1;
-  __syncthreads();
+}
 
-  // Pass 2: stable placement, walking the warp's range in order.
-  for (int b = lo; b < hi; b += 32 * kUnroll) {
-    int e[kUnroll];
-#pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const int p = b + j * 32 + lane;
-      const int v = (p < hi) ? __ldg(ids + p) : -1;
-      e[j] = (v >= 0 && v < E) ? v : -1;
+__global__ void __launch_bounds__(kAlignThreads)
+    align_scatter_kernel(const int32_t* __restrict__ ids, int num_pairs, int E, int chunk,
+                         const int32_t* __restrict__ chunk_base, int* __restrict__ done,
+                         int32_t* __restrict__ sorted_ids) {
+  extern __shared__ int cur[];  // [kAlignWarps][E]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) cur[i] = 0;
+  if (blockIdx.x == 0 && tid == 0) *done = 0;  // the count kernel of the next call starts from zero
+  __syncthreads();
+  const int lo = blockIdx.x * chunk;
+  const int span = chunk / kAlignWarps;  // multiple of 32
+  const int wlo = min(num_pairs, lo + warp * span);
+  const int whi = min(num_pairs, wlo + span);
+  // per-warp counts of its slice
+  for (int b = wlo; b < whi; b += 32) {
+    const int p = b + lane;
+    const int v = (p < whi) ? __ldg(ids + p) : -1;
+    if (v >= 0 && v < E) atomicAdd(&cur[warp * E + v], 1);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kAlignThreads) {
+    int run = __ldg(chunk_base + static_cast<size_t>(blockIdx.x) * E + e);
+    for (int w = 0; w < kAlignWarps; ++w) {
+      const int n = cur[w * E + e];
+      cur[w * E + e] = run;
+      run += n;
     }
-#pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const int p = b + j * 32 + lane;
-      const uint32_t peers = __match_any_sync(0xffffffffu, e[j]);
-      int base = 0;
-      if (e[j] >= 0) base = cur[warp * E + e[j]];
-      __syncwarp();
-      if (e[j] >= 0) {
-        sorted_ids[base + __popc(peers & lt_mask)] = p;
-        if ((peers & lt_mask) == 0) cur[warp * E + e[j]] = base + __popc(peers);
-      }
-      __syncwarp();
+  }
+  __syncthreads();
+  for (int b = wlo; b < whi; b += 32) {
+    const int p = b + lane;
+    int e = (p < whi) ? __ldg(ids + p) : -1;
+    if (e >= E) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int base = 0;
+    if (e >= 0) base = cur[warp * E + e];
+    __syncwarp();
+    if (e >= 0) {
+      sorted_ids[base + __popc(peers & lt_mask)] = p;
+      if ((peers & lt_mask) == 0) cur[warp * E + e] = base + __popc(peers);
     }
+    __syncwarp();
   }
 }
 
@@ -147,16 +172,30 @@ size_t align_max_padded(int num_pairs, int E, int block_m) {
 
 bool valid_block_m(int bm) { return bm >= 1 && bm <= 256 && (bm & (bm - 1)) == 0; }
 
-size_t align_smem_bytes(int E) { return static_cast<size_t>(kAlignWarps) * E * sizeof(int); }
+// Scratch of the align kernels: the completion ticket (256 bytes), then the chunk histograms.
+size_t align_scratch_bytes(int num_pairs, int E) {
+  const AlignPlan p = align_plan(num_pairs);
+  return 256 + align_up(static_cast<size_t>(p.nchunks) * E * 4, 256);
+}
 
 moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m, int32_t* sorted_ids,
-                          int32_t* expert_ids, int32_t* expert_offsets, int32_t* ntpp, int* err, cudaStream_t s) {
+                          int32_t* expert_ids, int32_t* expert_offsets, int32_t* ntpp, void* scratch, int* err,
+                          cudaStream_t s) {
   const int cap = static_cast<int>(align_max_padded(num_pairs, E, block_m));
-  const size_t smem = align_smem_bytes(E);
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(align_kernel), static_cast<int>(align_smem_bytes(MOE_MAX_EXPERTS))))
+  const AlignPlan p = align_plan(num_pairs);
+  int* done = static_cast<int*>(scratch);
+  int32_t* chunk_base = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + 256);
+  align_count_scan_kernel<<<p.nchunks, kAlignThreads, 0, s>>>(ids, num_pairs, E, block_m, cap, p.chunk, p.nchunks,
+                                                              chunk_base, done, sorted_ids, expert_ids,
+                                                              expert_offsets, ntpp, err);
+  moe_status_t st = launch_status();
+  if (st != MOE_OK) return st;
+  const size_t smem = static_cast<size_t>(kAlignWarps) * E * sizeof(int);
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(align_scatter_kernel),
+                        static_cast<int>(static_cast<size_t>(kAlignWarps) * MOE_MAX_EXPERTS * sizeof(int))))
     return MOE_ERR_CUDA;
-  align_kernel<<<1, kAlignThreads, smem, s>>>(ids, num_pairs, E, block_m, cap, sorted_ids, expert_ids,
-                                              expert_offsets, ntpp, err);
+  align_scatter_kernel<<<p.nchunks, kAlignThreads, smem, s>>>(ids, num_pairs, E, p.chunk, chunk_base, done,
+                                                              sorted_ids);
   return launch_status();
 }
 
@@ -167,8 +206,8 @@ extern "C" size_t moe_align_max_padded(int num_pairs, int E, int block_m) {
 }
 
 extern "C" size_t moe_align_workspace_size(int num_pairs, int E, int block_m) {
-  (void)num_pairs; (void)E; (void)block_m;
-  return moe::kWsHeader;
+  if (num_pairs < 0 || E < 1 || !moe::valid_block_m(block_m)) return 0;
+  return moe::kWsHeader + moe::align_scratch_bytes(num_pairs, E);
 }
 
 extern "C" moe_status_t moe_align_block_size(const int32_t* topk_ids, int num_pairs, int E, int block_m,
@@ -180,7 +219,11 @@ extern "C" moe_status_t moe_align_block_size(const int32_t* topk_ids, int num_pa
   if ((num_pairs > 0 && !topk_ids) || (!empty && (!sorted_token_ids || !expert_ids)) || !expert_offsets ||
       !num_tokens_post_padded)
     return MOE_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < moe_align_workspace_size(num_pairs, E, block_m)) return MOE_ERR_WORKSPACE;
+  if (!ws || ws_bytes < moe_align_workspace_size(num_pairs, E, block_m) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return MOE_ERR_WORKSPACE;
+  uint8_t* w = static_cast<uint8_t*>(ws);
   return moe::launch_align(topk_ids, num_pairs, E, block_m, sorted_token_ids, expert_ids, expert_offsets,
-                           num_tokens_post_padded, static_cast<int*>(ws), moe::as_stream(stream));
+                           num_tokens_post_padded, w + moe::kWsHeader, reinterpret_cast<int*>(w),
+                           moe::as_stream(stream));
 }

@@ -17,8 +17,10 @@ moe_status_t validate_routing(int T, int E, int G, int kg, int k, int scoring);
 moe_status_t launch_grouped_topk(const float* gating, int T, int E, int G, int kg, int k, int scoring, int renorm,
                                  float rsf, float* w, int32_t* ids, cudaStream_t s);
 size_t align_max_padded(int num_pairs, int E, int block_m);
+size_t align_scratch_bytes(int num_pairs, int E);
 moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m, int32_t* sorted_ids,
-                          int32_t* expert_ids, int32_t* expert_offsets, int32_t* ntpp, int* err, cudaStream_t s);
+                          int32_t* expert_ids, int32_t* expert_offsets, int32_t* ntpp, void* scratch, int* err,
+                          cudaStream_t s);
 moe_status_t launch_gemm_gate_up(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_ids,
                                  const int32_t* expert_ids, const int32_t* ntpp, __nv_bfloat16* h, int* err,
                                  int num_pairs, int topk, int H, int I, int E, cudaStream_t s);
@@ -47,7 +49,7 @@ __global__ void cast_f32_bf16_kernel(const float4* __restrict__ src, uint2* __re
 }
 
 struct FusedLayout {
-  size_t sorted_ids, expert_ids, expert_offsets, ntpp, h, y_acc, total;
+  size_t align_scratch, sorted_ids, expert_ids, expert_offsets, ntpp, h, y_acc, total;
   int cap;
 };
 
@@ -56,6 +58,7 @@ FusedLayout fused_layout(int T, int H, int I, int E, int topk) {
   const int num_pairs = T * topk;
   L.cap = static_cast<int>(align_max_padded(num_pairs, E, kBlockM));
   size_t off = kWsHeader;
+  L.align_scratch = off; off = align_up(off + align_scratch_bytes(num_pairs, E), 256);
   L.sorted_ids = off; off = align_up(off + static_cast<size_t>(L.cap) * 4, 256);
   L.expert_ids = off; off = align_up(off + static_cast<size_t>(L.cap / kBlockM + 1) * 4, 256);
   L.expert_offsets = off; off = align_up(off + static_cast<size_t>(E + 1) * 4, 256);
@@ -129,7 +132,8 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
                            routed_scaling_factor, topk_weights, topk_ids, s);
   if (st != MOE_OK) return st;
   stage_mark(1, s);
-  st = launch_align(topk_ids, num_pairs, E, kBlockM, sorted_ids, expert_ids, offsets, ntpp, err, s);
+  st = launch_align(topk_ids, num_pairs, E, kBlockM, sorted_ids, expert_ids, offsets, ntpp, w + L.align_scratch, err,
+                    s);
   if (st != MOE_OK) return st;
   stage_mark(2, s);
   const size_t n4 = static_cast<size_t>(T) * H / 4;

@@ -7,10 +7,11 @@
 // increasing, so groups and experts are selected on the logits themselves and
 // only the k selected logits are exponentiated when the weights renormalise.
 //
-// Lane l holds the logits of experts [l*VPL, (l+1)*VPL). Selection keys are the
-// logits mapped to order-preserving unsigned integers; warp-wide maxima and the
-// lowest index among equal maxima come from redux.sync, so ties resolve to the
-// lower expert (or group) index.
+// Lane l holds the logits of experts [l*VPL, (l+1)*VPL). Warp-wide maxima and
+// the lowest index among equal maxima come from redux.sync, so ties resolve to
+// the lower expert (or group) index. The fast kernel (E = 32*VPL, power-of-two
+// group count) reduces the float logits directly; the generic kernel (any E and
+// G) reduces order-preserving unsigned keys of the logits.
 #include "common.cuh"
 
 #include <cuda_runtime.h>
@@ -33,6 +34,131 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
+}
+
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// Weights of the k selections held by lanes 0..k-1 (blog 3.6 / section 七).
+__device__ __forceinline__ float route_weight(float x, bool active, const float* v, int nv, int base, int E,
+                                              int scoring, int renorm, float rsf) {
+  float w;
+  if (scoring == MOE_SCORE_SOFTMAX) {
+    if (renorm) {
+      // softmax over the selected logits only: the full denominator cancels
+      const float x0 = __shfl_sync(0xffffffffu, x, 0);
+      const float ex = active ? expf(x - x0) : 0.f;
+      w = ex / warp_sum(ex);
+    } else {
+      float lmax = -CUDART_INF_F;
+#pragma unroll
+      for (int j = 0; j < nv; ++j)
+        if (base + j < E) lmax = fmaxf(lmax, v[j]);
+      const float gmax = warp_max_f32(lmax);
+      float part = 0.f;
+#pragma unroll
+      for (int j = 0; j < nv; ++j)
+        if (base + j < E) part += expf(v[j] - gmax);
+      const float den = warp_sum(part);
+      w = active ? expf(x - gmax) / den : 0.f;
+    }
+  } else {
+    const float sg = active ? 1.0f / (1.0f + expf(-x)) : 0.f;
+    w = renorm ? sg / warp_sum(sg) : sg;
+  }
+  return w * rsf;
+}
+
+// Fast path: E = 32 * VPL and G a power of two (a group spans 32 / G whole lanes).
+// Group maxima come from segmented shuffles, group selection from each group's
+// rank (no serial chain), and each lane caches its best two candidates so that
+// only a lane that wins twice rescans its logits.
+template <int VPL>
+__global__ void __launch_bounds__(256) grouped_topk_fast_kernel(const float* __restrict__ gating, int T, int G,
+                                                                int topk_group, int topk, int scoring, int renorm,
+                                                                float rsf, float* __restrict__ out_w,
+                                                                int32_t* __restrict__ out_ids) {
+  constexpr int E = 32 * VPL;
+  const int token = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (token >= T) return;
+  const float* row = gating + static_cast<size_t>(token) * E;
+  const int base = lane * VPL;
+  float v[VPL];
+  if constexpr (VPL % 4 == 0) {
+#pragma unroll
+    for (int q = 0; q < VPL / 4; ++q) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(row + base) + q);
+      v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) v[j] = __ldg(row + base + j);
+  }
+
+  // 3.2 / 3.3: group maximum over the group's lanes, then the group's rank.
+  bool selected = true;
+  if (G > 1) {
+    const int lpg = 32 / G;
+    float gk = v[0];
+#pragma unroll
+    for (int j = 1; j < VPL; ++j) gk = fmaxf(gk, v[j]);
+    for (int o = 1; o < lpg; o <<= 1) gk = fmaxf(gk, __shfl_xor_sync(0xffffffffu, gk, o));
+    const int my_g = lane / lpg;
+    int rank = 0;
+    for (int g = 0; g < G; ++g) {
+      const float o = __shfl_sync(0xffffffffu, gk, g * lpg);
+      rank += (o > gk || (o == gk && g < my_g)) ? 1 : 0;
+    }
+    selected = rank < topk_group;
+  }
+
+  // 3.4 / 3.5: the lane's best two candidates (ties keep the lower index).
+  float best = -CUDART_INF_F, second = -CUDART_INF_F;
+  int bidx = 0x7fffffff, sidx = 0x7fffffff;
+  uint32_t taken = 0;
+  if (selected) {
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      if (v[j] > best) { second = best; sidx = bidx; best = v[j]; bidx = base + j; }
+      else if (v[j] > second) { second = v[j]; sidx = base + j; }
+    }
+  }
+  bool second_valid = true;
+  float my_x = 0.f;
+  int my_id = 0;
+  for (int it = 0; it < topk; ++it) {
+    const float m = warp_max_f32(best);
+    const uint32_t w = __reduce_min_sync(0xffffffffu, best == m ? static_cast<uint32_t>(bidx) : 0x7fffffffu);
+    if (lane == it) { my_x = m; my_id = static_cast<int>(w); }
+    if (bidx == static_cast<int>(w) && w != 0x7fffffffu) {
+      taken |= 1u << (bidx - base);
+      if (second_valid) {
+        best = second; bidx = sidx;
+        second_valid = false;
+      } else {
+        best = -CUDART_INF_F; bidx = 0x7fffffff;
+        second = -CUDART_INF_F; sidx = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+          if ((taken >> j) & 1u) continue;
+          if (v[j] > best) { second = best; sidx = bidx; best = v[j]; bidx = base + j; }
+          else if (v[j] > second) { second = v[j]; sidx = base + j; }
+        }
+        second_valid = true;
+      }
+    }
+  }
+
+  const bool active = lane < topk;
+  const float wgt = route_weight(my_x, active, v, VPL, base, E, scoring, renorm, rsf);
+  if (active) {
+    out_w[static_cast<size_t>(token) * topk + lane] = wgt;
+    out_ids[static_cast<size_t>(token) * topk + lane] = my_id;
+  }
 }
 
 template <int VPL>
@@ -71,6 +197,15 @@ __global__ void __launch_bounds__(256) grouped_topk_kernel(const float* __restri
   uint32_t key[VPL];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) key[j] = (base + j < E) ? order_key(v[j]) : 0u;
+  int grp[VPL];  // group of each of the lane's experts, without a division per element
+  {
+    int g = base / P, next = (base / P + 1) * P;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      if (base + j >= next) { ++g; next += P; }
+      grp[j] = g;
+    }
+  }
 
   // 3.2: group maxima. Lane g (< G) ends up holding the key of group g.
   uint32_t my_gkey = 0;
@@ -89,7 +224,7 @@ __global__ void __launch_bounds__(256) grouped_topk_kernel(const float* __restri
       uint32_t lmax = 0;
 #pragma unroll
       for (int j = 0; j < VPL; ++j)
-        if ((base + j) / P == g) lmax = max(lmax, key[j]);
+        if (grp[j] == g) lmax = max(lmax, key[j]);
       const uint32_t m = __reduce_max_sync(0xffffffffu, lmax);
       if (lane == g) my_gkey = m;
     }
@@ -111,8 +246,7 @@ __global__ void __launch_bounds__(256) grouped_topk_kernel(const float* __restri
   // 3.4: mask experts of unselected groups (key 0 is below every finite logit).
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
-    const int e = base + j;
-    if (e < E && !((sel_groups >> (e / P)) & 1u)) key[j] = 0u;
+    if (base + j < E && !((sel_groups >> grp[j]) & 1u)) key[j] = 0u;
   }
 
   // 3.5: top `topk` experts (ties -> lower expert index).
@@ -174,6 +308,14 @@ __global__ void __launch_bounds__(256) grouped_topk_kernel(const float* __restri
 }
 
 template <int VPL>
+void launch_fast(const float* gating, int T, int G, int kg, int k, int scoring, int renorm, float rsf, float* w,
+                 int32_t* ids, cudaStream_t s) {
+  const int threads = 256;
+  const int blocks = cdiv(T, threads / 32);
+  grouped_topk_fast_kernel<VPL><<<blocks, threads, 0, s>>>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids);
+}
+
+template <int VPL>
 void launch_topk(const float* gating, int T, int E, int G, int kg, int k, int scoring, int renorm, float rsf,
                  float* w, int32_t* ids, cudaStream_t s) {
   const int threads = 256;
@@ -194,6 +336,18 @@ moe_status_t validate_routing(int T, int E, int G, int kg, int k, int scoring) {
 moe_status_t launch_grouped_topk(const float* gating, int T, int E, int G, int kg, int k, int scoring, int renorm,
                                  float rsf, float* w, int32_t* ids, cudaStream_t s) {
   if (T == 0) return MOE_OK;
+  const bool pow2_groups = (G & (G - 1)) == 0;
+  if (pow2_groups) {
+    switch (E) {
+      case 32: launch_fast<1>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, s); return launch_status();
+      case 64: launch_fast<2>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, s); return launch_status();
+      case 128: launch_fast<4>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, s); return launch_status();
+      case 256: launch_fast<8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, s); return launch_status();
+      case 512: launch_fast<16>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, s); return launch_status();
+      case 1024: launch_fast<32>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, s); return launch_status();
+      default: break;
+    }
+  }
   const int per_lane = cdiv(E, 32);
   if (per_lane <= 1) launch_topk<1>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, s);
   else if (per_lane <= 2) launch_topk<2>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, s);

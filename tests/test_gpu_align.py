@@ -18,8 +18,10 @@ def _gpu():
 def _check(ids_np, E, bm):
     import mixture_experts_routing_grouped_gb300 as moe
     ids = torch.from_numpy(np.ascontiguousarray(ids_np, dtype=np.int32)).cuda()
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(moe.lib().moe_align_workspace_size(ids.numel(), E, bm), dtype=torch.uint8, device="cuda")
     s, eids, off, ntpp = moe.moe_align_block_size(ids, bm, E, ws=ws)
+    s2, _, _, _ = moe.moe_align_block_size(ids, bm, E, ws=ws)   # the workspace is reusable as left
+    assert torch.equal(s, s2)
     torch.cuda.synchronize()
     rs, reids, roff, rtotal = align.moe_align_block_size(ids_np, bm, E)
     assert int(ntpp.item()) == rtotal
@@ -57,7 +59,7 @@ def test_align_out_of_range_ids_are_skipped_and_reported():
     import mixture_experts_routing_grouped_gb300 as moe
     ids_np = np.array([3, 9, 1, -1, 3, 0, 7], dtype=np.int32)   # 9 and -1 are outside [0, 8)
     ids = torch.from_numpy(ids_np).cuda()
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(moe.lib().moe_align_workspace_size(7, 8, 4), dtype=torch.uint8, device="cuda")
     s, eids, off, ntpp = moe.moe_align_block_size(ids, 4, 8, ws=ws)
     code = moe.moe_check_device_error(ws)
     assert code & moe.DEVERR_EXPERT_ID

@@ -74,6 +74,9 @@ def test_align_validation(L):
     assert f(FAKE, 10, 0, 4, FAKE, FAKE, FAKE, FAKE, FAKE, 4096, None) == 1
     assert f(FAKE, 10, 8, 4, FAKE, FAKE, FAKE, FAKE, None, 4096, None) == 3   # no workspace
     assert f(FAKE, 10, 8, 4, FAKE, FAKE, FAKE, FAKE, FAKE, 8, None) == 3      # workspace too small
+    need = L.moe_align_workspace_size(10, 8, 4)
+    assert need > 256
+    assert f(FAKE, 10, 8, 4, FAKE, FAKE, FAKE, FAKE, FAKE, need - 1, None) == 3
 
 
 def test_fused_validation_and_sizes(L):
