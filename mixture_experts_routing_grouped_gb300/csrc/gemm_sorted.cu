@@ -44,7 +44,9 @@ constexpr int kEpiThreads = 128;
 constexpr int kProdThreads = 128;
 constexpr int kGemmThreads = kEpiThreads + kProdThreads + 32;
 constexpr int kTmemCols = 2 * kBN;
-constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 256 + 4 * kBM * 4;
+constexpr int kStagePitch = 36;  // floats per staged row (16-byte aligned, few bank conflicts)
+constexpr size_t kEpiStageBytes = 4 * 32 * kStagePitch * 4;
+constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 256 + 4 * kBM * 4 + kEpiStageBytes;
 static_assert(kStages == 4, "one producer warp per ring slot");
 
 enum GemmMode { kGateUp = 0, kDown = 1 };
@@ -241,6 +243,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    // Each warp drains its 32 accumulator rows 32 columns at a time through a
+    // shared staging tile, so that the global stores (gate_up) and the fp32
+    // atomics (down) of one instruction cover whole row segments of 4-8 rows
+    // instead of 32 scattered 16-byte pieces.
+    float* stg = reinterpret_cast<float*>(ctl + 256 + 4 * kBM * 4) + warp * 32 * kStagePitch;
     const int r = warp * 32 + lane;  // accumulator row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     int it = 0;
@@ -255,45 +262,61 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + lane_off + b * kBN;
       if (MODE == kGateUp) {
+        // h[pos, n0 + c*32 .. +32] = silu(gate) * up; 8 lanes write one row's 64 bytes
         const int n0 = nt * kBM;
-        __nv_bfloat16* hrow = args.h + static_cast<size_t>(pos) * args.I + n0;
+        const int row0 = mt * kBM + warp * 32;
 #pragma unroll 1
         for (int c = 0; c < kBM / 32; ++c) {
           uint32_t g[32], u[32];
           ptx::tmem_ld32(tbase + c * 32, g);
           ptx::tmem_ld32(tbase + kBM + c * 32, u);
           ptx::tmem_ld_wait();
-          uint32_t packed[16];
+          uint32_t* srow = reinterpret_cast<uint32_t*>(stg + lane * kStagePitch);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
             const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
             const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
-            packed[j] = *reinterpret_cast<const uint32_t*>(&hv);
+            srow[j] = *reinterpret_cast<const uint32_t*>(&hv);
           }
-          uint4* dst = reinterpret_cast<uint4*>(hrow + c * 32);
+          __syncwarp();
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+          for (int i = 0; i < 8; ++i) {
+            const int rl = i * 4 + (lane >> 3);
+            const int q = lane & 7;  // 8 bytes of the row's 64
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(stg + rl * kStagePitch) + 2 * q;
+            uint2* dst = reinterpret_cast<uint2*>(args.h + static_cast<size_t>(row0 + rl) * args.I + n0 + c * 32) + q;
+            *dst = make_uint2(src[0], src[1]);
+          }
+          __syncwarp();
         }
       } else {
         const bool valid = sid < args.num_pairs;
         const float w = valid ? __ldg(args.topk_w + sid) : 0.f;
-        const int tok = valid ? sid / args.topk : 0;
-        float* yrow = args.y_acc + static_cast<size_t>(tok) * args.H + nt * kBN;
+        const int tok = valid ? sid / args.topk : -1;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t d[32];
           ptx::tmem_ld32(tbase + c * 32, d);
           ptx::tmem_ld_wait();
-          if (valid) {
+          float4* srow = reinterpret_cast<float4*>(stg + lane * kStagePitch);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 v = make_float4(w * __uint_as_float(d[4 * q]), w * __uint_as_float(d[4 * q + 1]),
-                                           w * __uint_as_float(d[4 * q + 2]), w * __uint_as_float(d[4 * q + 3]));
-              atomicAdd(reinterpret_cast<float4*>(yrow + c * 32 + 4 * q), v);
-            }
+          for (int q = 0; q < 8; ++q)
+            srow[q] = make_float4(w * __uint_as_float(d[4 * q]), w * __uint_as_float(d[4 * q + 1]),
+                                  w * __uint_as_float(d[4 * q + 2]), w * __uint_as_float(d[4 * q + 3]));
+          __syncwarp();
+          // 8 lanes add one row's 32 floats (128 contiguous bytes) into its token row
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rl = i * 4 + (lane >> 3);
+            const int q = lane & 7;
+            const int trow = __shfl_sync(0xffffffffu, tok, rl);
+            const float4 v = reinterpret_cast<const float4*>(stg + rl * kStagePitch)[q];
+            if (trow >= 0)
+              atomicAdd(reinterpret_cast<float4*>(args.y_acc + static_cast<size_t>(trow) * args.H + nt * kBN +
+                                                  c * 32) + q, v);
           }
+          __syncwarp();
         }
       }
       ptx::tc_fence_before();
