@@ -11,6 +11,10 @@
 // on the padded length is replaced by a device-side length read by the GEMMs.
 #include "common.cuh"
 
+#include <cstdlib>
+#include <cstring>
+#include <algorithm>
+
 namespace moe {
 
 moe_status_t validate_routing(int T, int E, int G, int kg, int k, int scoring);
@@ -28,9 +32,41 @@ moe_status_t launch_gemm_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, c
                               const int32_t* expert_ids, const int32_t* ntpp, const float* topk_w, float* y_acc,
                               int* err, int num_pairs, int topk, int cap, int H, int I, int E, cudaStream_t s);
 
+moe_status_t launch_swap_gate_up(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_ids,
+                                 const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk, int H,
+                                 int I, int E, int nmax, cudaStream_t s);
+moe_status_t launch_swap_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, const int32_t* sorted_ids,
+                              const int32_t* offsets, const float* topk_w, float* y_acc, int* err, int num_pairs,
+                              int topk, int cap, int H, int I, int E, int nmax, cudaStream_t s);
+
 namespace {
 
-constexpr int kBlockM = 128;
+// Kernel choice. Decode-sized problems (at most 32 rows per expert on average)
+// use the swap-AB kernels with 16-row blocks and token tiles of <= 32; larger
+// ones use the sorted-layout kernels with 128-row blocks, unless the
+// MOE_GB300_PREFILL_KERNEL environment variable says "swap" (token tiles of
+// <= 256 on 16-row blocks) -- a switch for comparing the two on one workload.
+struct Plan {
+  bool swap;
+  int nmax;
+  int block_m;
+};
+
+Plan choose_plan(int T, int E, int topk) {
+  Plan p{};
+  const long long pairs = static_cast<long long>(T) * topk;
+  if (pairs <= 32ll * E) {
+    p.swap = true; p.nmax = 32; p.block_m = 16;
+  } else {
+    const char* env = std::getenv("MOE_GB300_PREFILL_KERNEL");
+    if (env && std::strcmp(env, "swap") == 0) {
+      p.swap = true; p.nmax = 256; p.block_m = 16;
+    } else {
+      p.swap = false; p.nmax = 0; p.block_m = 128;
+    }
+  }
+  return p;
+}
 
 __global__ void zero_f32_kernel(float4* __restrict__ p, size_t n4) {
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
@@ -53,14 +89,14 @@ struct FusedLayout {
   int cap;
 };
 
-FusedLayout fused_layout(int T, int H, int I, int E, int topk) {
+FusedLayout fused_layout(int T, int H, int I, int E, int topk, int block_m) {
   FusedLayout L{};
   const int num_pairs = T * topk;
-  L.cap = static_cast<int>(align_max_padded(num_pairs, E, kBlockM));
+  L.cap = static_cast<int>(align_max_padded(num_pairs, E, block_m));
   size_t off = kWsHeader;
   L.align_scratch = off; off = align_up(off + align_scratch_bytes(num_pairs, E), 256);
   L.sorted_ids = off; off = align_up(off + static_cast<size_t>(L.cap) * 4, 256);
-  L.expert_ids = off; off = align_up(off + static_cast<size_t>(L.cap / kBlockM + 1) * 4, 256);
+  L.expert_ids = off; off = align_up(off + static_cast<size_t>(L.cap / block_m + 1) * 4, 256);
   L.expert_offsets = off; off = align_up(off + static_cast<size_t>(E + 1) * 4, 256);
   L.ntpp = off; off = align_up(off + 4, 1024);
   L.h = off; off = align_up(off + static_cast<size_t>(L.cap) * I * 2, 1024);
@@ -92,7 +128,8 @@ extern "C" void moe_set_stage_events(void* const* events, int n) {
 
 extern "C" size_t moe_fused_forward_workspace_size(int T, int H, int I, int E, int topk) {
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0) return 0;
-  return moe::fused_layout(T, H, I, E, topk).total;
+  // large enough for either kernel family
+  return std::max(moe::fused_layout(T, H, I, E, topk, 16).total, moe::fused_layout(T, H, I, E, topk, 128).total);
 }
 
 extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, const void* w_gate_up,
@@ -112,8 +149,9 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   if (T == 0) return MOE_OK;
   if (static_cast<long long>(T) * topk >= (1ll << 30) || static_cast<long long>(T) * H >= (1ll << 31))
     return MOE_ERR_UNSUPPORTED;
-  const FusedLayout L = fused_layout(T, H, I, E, topk);
-  if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+  const Plan plan = choose_plan(T, E, topk);
+  const FusedLayout L = fused_layout(T, H, I, E, topk, plan.block_m);
+  if (!ws || ws_bytes < moe_fused_forward_workspace_size(T, H, I, E, topk) || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
   if (T == 0) return MOE_OK;
 
   cudaStream_t s = as_stream(stream);
@@ -132,20 +170,28 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
                            routed_scaling_factor, topk_weights, topk_ids, s);
   if (st != MOE_OK) return st;
   stage_mark(1, s);
-  st = launch_align(topk_ids, num_pairs, E, kBlockM, sorted_ids, expert_ids, offsets, ntpp, w + L.align_scratch, err,
-                    s);
+  st = launch_align(topk_ids, num_pairs, E, plan.block_m, sorted_ids, expert_ids, offsets, ntpp, w + L.align_scratch,
+                    err, s);
   if (st != MOE_OK) return st;
   stage_mark(2, s);
   const size_t n4 = static_cast<size_t>(T) * H / 4;
   zero_f32_kernel<<<grid_for(n4), 256, 0, s>>>(reinterpret_cast<float4*>(y_acc), n4);
   if ((st = launch_status()) != MOE_OK) return st;
   stage_mark(3, s);
-  st = launch_gemm_gate_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_gate_up),
-                           sorted_ids, expert_ids, ntpp, h, err, num_pairs, topk, H, I, E, s);
+  if (plan.swap)
+    st = launch_swap_gate_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_gate_up),
+                             sorted_ids, offsets, h, err, num_pairs, topk, H, I, E, plan.nmax, s);
+  else
+    st = launch_gemm_gate_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_gate_up),
+                             sorted_ids, expert_ids, ntpp, h, err, num_pairs, topk, H, I, E, s);
   if (st != MOE_OK) return st;
   stage_mark(4, s);
-  st = launch_gemm_down(h, static_cast<const __nv_bfloat16*>(w_down), sorted_ids, expert_ids, ntpp, topk_weights,
-                        y_acc, err, num_pairs, topk, L.cap, H, I, E, s);
+  if (plan.swap)
+    st = launch_swap_down(h, static_cast<const __nv_bfloat16*>(w_down), sorted_ids, offsets, topk_weights, y_acc, err,
+                          num_pairs, topk, L.cap, H, I, E, plan.nmax, s);
+  else
+    st = launch_gemm_down(h, static_cast<const __nv_bfloat16*>(w_down), sorted_ids, expert_ids, ntpp, topk_weights,
+                          y_acc, err, num_pairs, topk, L.cap, H, I, E, s);
   if (st != MOE_OK) return st;
   stage_mark(5, s);
   cast_f32_bf16_kernel<<<grid_for(n4), 256, 0, s>>>(reinterpret_cast<const float4*>(y_acc),
