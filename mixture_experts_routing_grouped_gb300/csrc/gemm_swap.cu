@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float g = __uint_as_float(v0[j]);
-            hstage[j * kSwM + i] = __float2bfloat16_rn(g / (1.0f + __expf(-g)) * __uint_as_float(v1[j]));
+            hstage[j * kSwM + i] = __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(v1[j]));
           }
           asm volatile("bar.sync 1, 128;" ::: "memory");
           // 16 lanes store one token's 256 bytes: a warp covers 2 tokens per instruction
