@@ -25,9 +25,9 @@ size_t align_scratch_bytes(int num_pairs, int E);
 moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m, int32_t* sorted_ids,
                           int32_t* expert_ids, int32_t* expert_offsets, int32_t* ntpp, void* scratch, int* err,
                           cudaStream_t s);
-moe_status_t launch_gemm_gate_up(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_ids,
-                                 const int32_t* expert_ids, const int32_t* ntpp, __nv_bfloat16* h, int* err,
-                                 int num_pairs, int topk, int H, int I, int E, cudaStream_t s);
+moe_status_t launch_gemm_gate_up_pairs(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_ids,
+                                       const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
+                                       int H, int I, int E, cudaStream_t s);
 moe_status_t launch_gemm_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, const int32_t* sorted_ids,
                               const int32_t* expert_ids, const int32_t* ntpp, const float* topk_w, float* y_acc,
                               int* err, int num_pairs, int topk, int cap, int H, int I, int E, cudaStream_t s);
@@ -182,8 +182,9 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
     st = launch_swap_gate_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_gate_up),
                              sorted_ids, offsets, h, err, num_pairs, topk, H, I, E, plan.nmax, s);
   else
-    st = launch_gemm_gate_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_gate_up),
-                             sorted_ids, expert_ids, ntpp, h, err, num_pairs, topk, H, I, E, s);
+    st = launch_gemm_gate_up_pairs(static_cast<const __nv_bfloat16*>(x),
+                                   static_cast<const __nv_bfloat16*>(w_gate_up), sorted_ids, offsets, h, err,
+                                   num_pairs, topk, H, I, E, s);
   if (st != MOE_OK) return st;
   stage_mark(4, s);
   if (plan.swap)
