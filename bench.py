@@ -194,7 +194,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
         torch.distributed.barrier()
     clk = clocks.stop()
     step_ms = [ev[k][0].elapsed_time(ev[k][n_stage - 1]) for k in range(K)]
-    stage_names = ["routing", "align", "acc_clear", "gemm_gate_up", "gemm_down", "cast"]
+    stage_names = ["routing_and_clear", "align", "unused", "gemm_gate_up", "gemm_down", "cast"]
     stage_ms = {n: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
                 for i, n in enumerate(stage_names)}
     ms = statistics.mean(step_ms)
@@ -270,7 +270,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "e2e": {"value": round(world * cfg.T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": 6 * K,
+        "gpu_launches": 6 * K,  # routing, align count/scan, align scatter, gate_up, down, cast
         "clocks": clk,
     }
     if not args.skip_extra and world == 1:

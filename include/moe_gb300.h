@@ -181,8 +181,9 @@ MOE_API moe_status_t moe_fused_forward_noalloc(const void* x, const float* gatin
  * moe_set_stage_events -- optional per-stage timing of moe_fused_forward (not in the
  * pages; instrumentation only). While set, every moe_fused_forward call made by
  * the calling host thread records events[0] on its stream before the routing
- * kernel and events[i] after its i-th kernel: 1 routing, 2 align, 3 accumulator
- * clear, 4 gate_up GEMM, 5 down GEMM, 6 cast to bf16 (n >= 7 records all). The
+ * kernel and events[i] after its i-th step: 1 routing (which also clears the
+ * fp32 accumulator), 2 align, 3 (empty: kept for a stable numbering), 4 gate_up
+ * GEMM, 5 down GEMM, 6 cast to bf16 (n >= 7 records all). The
  * events are cudaEvent_t handles owned by the caller. events = NULL or n = 0
  * switches the recording off.
  */

@@ -19,7 +19,8 @@ namespace moe {
 
 moe_status_t validate_routing(int T, int E, int G, int kg, int k, int scoring);
 moe_status_t launch_grouped_topk(const float* gating, int T, int E, int G, int kg, int k, int scoring, int renorm,
-                                 float rsf, float* w, int32_t* ids, cudaStream_t s);
+                                 float rsf, float* w, int32_t* ids, cudaStream_t s, float* zero_rows, int zero_cols,
+                                 int* zero_cnt, int cnt_per_row);
 size_t align_max_padded(int num_pairs, int E, int block_m);
 size_t align_scratch_bytes(int num_pairs, int E);
 moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m, int32_t* sorted_ids,
@@ -66,12 +67,6 @@ Plan choose_plan(int T, int E, int topk) {
     }
   }
   return p;
-}
-
-__global__ void zero_f32_kernel(float4* __restrict__ p, size_t n4) {
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x)
-    p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __global__ void cast_f32_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
@@ -166,8 +161,9 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   const int num_pairs = T * topk;
 
   stage_mark(0, s);
+  // the routing kernel also clears each token's row of the fp32 accumulator
   st = launch_grouped_topk(gating, T, E, num_expert_group, topk_group, topk, scoring, renormalize,
-                           routed_scaling_factor, topk_weights, topk_ids, s);
+                           routed_scaling_factor, topk_weights, topk_ids, s, y_acc, H, nullptr, 0);
   if (st != MOE_OK) return st;
   stage_mark(1, s);
   st = launch_align(topk_ids, num_pairs, E, plan.block_m, sorted_ids, expert_ids, offsets, ntpp, w + L.align_scratch,
@@ -175,8 +171,6 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   if (st != MOE_OK) return st;
   stage_mark(2, s);
   const size_t n4 = static_cast<size_t>(T) * H / 4;
-  zero_f32_kernel<<<grid_for(n4), 256, 0, s>>>(reinterpret_cast<float4*>(y_acc), n4);
-  if ((st = launch_status()) != MOE_OK) return st;
   stage_mark(3, s);
   if (plan.swap)
     st = launch_swap_gate_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_gate_up),

@@ -36,6 +36,27 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Rows of the layer's fp32 accumulator (and per-row counters) that the routing
+// warp of a token clears on the way out, so that the fused forward needs no
+// separate clearing kernel. Null pointers: nothing to clear.
+struct RouteZero {
+  float4* rows;
+  int row_f4;      // float4s per token row
+  int* cnt;
+  int cnt_per_row;
+};
+
+__device__ __forceinline__ void zero_token_rows(const RouteZero& z, int token, int lane) {
+  if (z.rows) {
+    float4* r = z.rows + static_cast<size_t>(token) * z.row_f4;
+    for (int i = lane; i < z.row_f4; i += 32) r[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (z.cnt) {
+    int* c = z.cnt + static_cast<size_t>(token) * z.cnt_per_row;
+    for (int i = lane; i < z.cnt_per_row; i += 32) c[i] = 0;
+  }
+}
+
 __device__ __forceinline__ float warp_max_f32(float v) {
   float r;
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
@@ -80,7 +101,7 @@ template <int VPL>
 __global__ void __launch_bounds__(256) grouped_topk_fast_kernel(const float* __restrict__ gating, int T, int G,
                                                                 int topk_group, int topk, int scoring, int renorm,
                                                                 float rsf, float* __restrict__ out_w,
-                                                                int32_t* __restrict__ out_ids) {
+                                                                int32_t* __restrict__ out_ids, RouteZero zero) {
   constexpr int E = 32 * VPL;
   const int token = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -159,13 +180,14 @@ __global__ void __launch_bounds__(256) grouped_topk_fast_kernel(const float* __r
     out_w[static_cast<size_t>(token) * topk + lane] = wgt;
     out_ids[static_cast<size_t>(token) * topk + lane] = my_id;
   }
+  zero_token_rows(zero, token, lane);
 }
 
 template <int VPL>
 __global__ void __launch_bounds__(256) grouped_topk_kernel(const float* __restrict__ gating, int T, int E, int G,
                                                            int topk_group, int topk, int scoring, int renorm,
                                                            float rsf, float* __restrict__ out_w,
-                                                           int32_t* __restrict__ out_ids) {
+                                                           int32_t* __restrict__ out_ids, RouteZero zero) {
   const int token = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (token >= T) return;
@@ -305,22 +327,23 @@ __global__ void __launch_bounds__(256) grouped_topk_kernel(const float* __restri
     out_w[static_cast<size_t>(token) * topk + lane] = w;
     out_ids[static_cast<size_t>(token) * topk + lane] = my_id;
   }
+  zero_token_rows(zero, token, lane);
 }
 
 template <int VPL>
 void launch_fast(const float* gating, int T, int G, int kg, int k, int scoring, int renorm, float rsf, float* w,
-                 int32_t* ids, cudaStream_t s) {
+                 int32_t* ids, const RouteZero& z, cudaStream_t s) {
   const int threads = 256;
   const int blocks = cdiv(T, threads / 32);
-  grouped_topk_fast_kernel<VPL><<<blocks, threads, 0, s>>>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids);
+  grouped_topk_fast_kernel<VPL><<<blocks, threads, 0, s>>>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z);
 }
 
 template <int VPL>
 void launch_topk(const float* gating, int T, int E, int G, int kg, int k, int scoring, int renorm, float rsf,
-                 float* w, int32_t* ids, cudaStream_t s) {
+                 float* w, int32_t* ids, const RouteZero& z, cudaStream_t s) {
   const int threads = 256;
   const int blocks = cdiv(T, threads / 32);
-  grouped_topk_kernel<VPL><<<blocks, threads, 0, s>>>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids);
+  grouped_topk_kernel<VPL><<<blocks, threads, 0, s>>>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z);
 }
 
 }  // namespace
@@ -334,27 +357,29 @@ moe_status_t validate_routing(int T, int E, int G, int kg, int k, int scoring) {
 }
 
 moe_status_t launch_grouped_topk(const float* gating, int T, int E, int G, int kg, int k, int scoring, int renorm,
-                                 float rsf, float* w, int32_t* ids, cudaStream_t s) {
+                                 float rsf, float* w, int32_t* ids, cudaStream_t s, float* zero_rows, int zero_cols,
+                                 int* zero_cnt, int cnt_per_row) {
   if (T == 0) return MOE_OK;
+  const RouteZero z{reinterpret_cast<float4*>(zero_rows), zero_cols / 4, zero_cnt, cnt_per_row};
   const bool pow2_groups = (G & (G - 1)) == 0;
   if (pow2_groups) {
     switch (E) {
-      case 32: launch_fast<1>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, s); return launch_status();
-      case 64: launch_fast<2>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, s); return launch_status();
-      case 128: launch_fast<4>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, s); return launch_status();
-      case 256: launch_fast<8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, s); return launch_status();
-      case 512: launch_fast<16>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, s); return launch_status();
-      case 1024: launch_fast<32>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, s); return launch_status();
+      case 32: launch_fast<1>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s); return launch_status();
+      case 64: launch_fast<2>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s); return launch_status();
+      case 128: launch_fast<4>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s); return launch_status();
+      case 256: launch_fast<8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s); return launch_status();
+      case 512: launch_fast<16>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s); return launch_status();
+      case 1024: launch_fast<32>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s); return launch_status();
       default: break;
     }
   }
   const int per_lane = cdiv(E, 32);
-  if (per_lane <= 1) launch_topk<1>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, s);
-  else if (per_lane <= 2) launch_topk<2>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, s);
-  else if (per_lane <= 4) launch_topk<4>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, s);
-  else if (per_lane <= 8) launch_topk<8>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, s);
-  else if (per_lane <= 16) launch_topk<16>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, s);
-  else launch_topk<32>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, s);
+  if (per_lane <= 1) launch_topk<1>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  else if (per_lane <= 2) launch_topk<2>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  else if (per_lane <= 4) launch_topk<4>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  else if (per_lane <= 8) launch_topk<8>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  else if (per_lane <= 16) launch_topk<16>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  else launch_topk<32>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
   return launch_status();
 }
 
@@ -368,5 +393,6 @@ extern "C" moe_status_t moe_grouped_topk(const float* gating, int T, int E, int 
   if (T > 0 && (!gating || !topk_weights || !topk_ids)) return MOE_ERR_INVALID_ARG;
   if (T > 0 && !moe::aligned16(gating)) return MOE_ERR_UNSUPPORTED;
   return moe::launch_grouped_topk(gating, T, E, num_expert_group, topk_group, topk, scoring, renormalize,
-                                  routed_scaling_factor, topk_weights, topk_ids, moe::as_stream(stream));
+                                  routed_scaling_factor, topk_weights, topk_ids, moe::as_stream(stream), nullptr, 0,
+                                  nullptr, 0);
 }
