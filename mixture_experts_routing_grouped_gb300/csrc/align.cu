@@ -18,7 +18,9 @@
 //     slice 32 pairs at a time, __match_any_sync groups lanes with the same
 //     expert and a pair's rank among them is the popcount of its lower peers.
 // Walking every range in order makes the sort stable; no atomics decide
-// positions.
+// positions. Optionally (the fused forward) the token of every sorted position,
+// pair / topk or -1 for padding, is written alongside, so that the grouped GEMMs
+// read gather rows without a division.
 #include "common.cuh"
 
 #include <algorithm>
@@ -46,8 +48,9 @@ AlignPlan align_plan(int num_pairs) {
 __global__ void __launch_bounds__(kAlignThreads)
     align_count_scan_kernel(const int32_t* __restrict__ ids, int num_pairs, int E, int block_m, int cap, int chunk,
                             int nchunks, int32_t* __restrict__ chunk_base, int* __restrict__ done,
-                            int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
-                            int32_t* __restrict__ expert_offsets, int32_t* __restrict__ ntpp, int* __restrict__ err) {
+                            int32_t* __restrict__ sorted_ids, int32_t* __restrict__ sorted_tok,
+                            int32_t* __restrict__ expert_ids, int32_t* __restrict__ expert_offsets,
+                            int32_t* __restrict__ ntpp, int* __restrict__ err) {
   __shared__ int hist[MOE_MAX_EXPERTS];
   __shared__ int warp_tot[kAlignWarps];
   __shared__ int is_last;
@@ -106,20 +109,26 @@ __global__ void __launch_bounds__(kAlignThreads)
       run += n;
     }
     for (int blk = start / block_m; blk < (start + padded) / block_m; ++blk) expert_ids[blk] = tid;
-    for (int pos = start + count; pos < start + padded; ++pos) sorted_ids[pos] = num_pairs;
+    for (int pos = start + count; pos < start + padded; ++pos) {
+      sorted_ids[pos] = num_pairs;
+      if (sorted_tok) sorted_tok[pos] = -1;
+    }
   }
   if (tid == 0) {
     expert_offsets[E] = total;
     *ntpp = total;
   }
-  for (int pos = total + tid; pos < cap; pos += kAlignThreads) sorted_ids[pos] = num_pairs;
+  for (int pos = total + tid; pos < cap; pos += kAlignThreads) {
+    sorted_ids[pos] = num_pairs;
+    if (sorted_tok) sorted_tok[pos] = -1;
+  }
   for (int blk = total / block_m + tid; blk < cap / block_m; blk += kAlignThreads) expert_ids[blk] = -1;
 }
 
 __global__ void __launch_bounds__(kAlignThreads)
     align_scatter_kernel(const int32_t* __restrict__ ids, int num_pairs, int E, int chunk,
                          const int32_t* __restrict__ chunk_base, int* __restrict__ done,
-                         int32_t* __restrict__ sorted_ids) {
+                         int32_t* __restrict__ sorted_ids, int32_t* __restrict__ sorted_tok, int topk) {
   extern __shared__ int cur[];  // [kAlignWarps][E]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
@@ -156,6 +165,7 @@ __global__ void __launch_bounds__(kAlignThreads)
     __syncwarp();
     if (e >= 0) {
       sorted_ids[base + __popc(peers & lt_mask)] = p;
+      if (sorted_tok) sorted_tok[base + __popc(peers & lt_mask)] = p / topk;
       if ((peers & lt_mask) == 0) cur[warp * E + e] = base + __popc(peers);
     }
     __syncwarp();
@@ -180,14 +190,14 @@ size_t align_scratch_bytes(int num_pairs, int E) {
 
 moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m, int32_t* sorted_ids,
                           int32_t* expert_ids, int32_t* expert_offsets, int32_t* ntpp, void* scratch, int* err,
-                          cudaStream_t s) {
+                          cudaStream_t s, int32_t* sorted_tok, int topk) {
   const int cap = static_cast<int>(align_max_padded(num_pairs, E, block_m));
   const AlignPlan p = align_plan(num_pairs);
   int* done = static_cast<int*>(scratch);
   int32_t* chunk_base = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + 256);
   align_count_scan_kernel<<<p.nchunks, kAlignThreads, 0, s>>>(ids, num_pairs, E, block_m, cap, p.chunk, p.nchunks,
-                                                              chunk_base, done, sorted_ids, expert_ids,
-                                                              expert_offsets, ntpp, err);
+                                                              chunk_base, done, sorted_ids, sorted_tok,
+                                                              expert_ids, expert_offsets, ntpp, err);
   moe_status_t st = launch_status();
   if (st != MOE_OK) return st;
   const size_t smem = static_cast<size_t>(kAlignWarps) * E * sizeof(int);
@@ -195,7 +205,7 @@ moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m,
                         static_cast<int>(static_cast<size_t>(kAlignWarps) * MOE_MAX_EXPERTS * sizeof(int))))
     return MOE_ERR_CUDA;
   align_scatter_kernel<<<p.nchunks, kAlignThreads, smem, s>>>(ids, num_pairs, E, p.chunk, chunk_base, done,
-                                                              sorted_ids);
+                                                              sorted_ids, sorted_tok, topk > 0 ? topk : 1);
   return launch_status();
 }
 
@@ -225,5 +235,5 @@ extern "C" moe_status_t moe_align_block_size(const int32_t* topk_ids, int num_pa
   uint8_t* w = static_cast<uint8_t*>(ws);
   return moe::launch_align(topk_ids, num_pairs, E, block_m, sorted_token_ids, expert_ids, expert_offsets,
                            num_tokens_post_padded, w + moe::kWsHeader, reinterpret_cast<int*>(w),
-                           moe::as_stream(stream));
+                           moe::as_stream(stream), nullptr, 0);
 }

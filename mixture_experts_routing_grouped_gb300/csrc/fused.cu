@@ -25,8 +25,12 @@ size_t align_max_padded(int num_pairs, int E, int block_m);
 size_t align_scratch_bytes(int num_pairs, int E);
 moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m, int32_t* sorted_ids,
                           int32_t* expert_ids, int32_t* expert_offsets, int32_t* ntpp, void* scratch, int* err,
-                          cudaStream_t s);
-moe_status_t launch_gemm_gate_up_pairs(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_ids,
+                          cudaStream_t s, int32_t* sorted_tok, int topk);
+moe_status_t launch_gemm_gate_up_pairs(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_tok,
+                                       const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
+                                       int H, int I, int E, cudaStream_t s);
+bool gate_up_pair2_supported(int I);
+moe_status_t launch_gemm_gate_up_pair2(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_tok,
                                        const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
                                        int H, int I, int E, cudaStream_t s);
 moe_status_t launch_gemm_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, const int32_t* sorted_ids,
@@ -44,11 +48,13 @@ namespace {
 
 // Kernel choice. Decode-sized problems (at most 32 rows per expert on average)
 // use the swap-AB kernels with 16-row blocks and token tiles of <= 32; larger
-// ones use the sorted-layout kernels with 128-row blocks, unless the
-// MOE_GB300_PREFILL_KERNEL environment variable says "swap" (token tiles of
-// <= 256 on 16-row blocks) -- a switch for comparing the two on one workload.
+// ones use the sorted-layout kernels with 128-row blocks. The
+// MOE_GB300_PREFILL_KERNEL environment variable selects another large-problem
+// kernel for comparisons on one workload: "swap" (token tiles of <= 256 on
+// 16-row blocks) or "cta_pair" (gate_up on CTA pairs, I a multiple of 256).
 struct Plan {
   bool swap;
+  bool pair_gate_up;
   int nmax;
   int block_m;
 };
@@ -64,6 +70,7 @@ Plan choose_plan(int T, int E, int topk) {
       p.swap = true; p.nmax = 256; p.block_m = 16;
     } else {
       p.swap = false; p.nmax = 0; p.block_m = 128;
+      p.pair_gate_up = env && std::strcmp(env, "cta_pair") == 0;
     }
   }
   return p;
@@ -80,7 +87,7 @@ __global__ void cast_f32_bf16_kernel(const float4* __restrict__ src, uint2* __re
 }
 
 struct FusedLayout {
-  size_t align_scratch, sorted_ids, expert_ids, expert_offsets, ntpp, h, y_acc, total;
+  size_t align_scratch, sorted_ids, sorted_tok, expert_ids, expert_offsets, ntpp, h, y_acc, total;
   int cap;
 };
 
@@ -91,6 +98,7 @@ FusedLayout fused_layout(int T, int H, int I, int E, int topk, int block_m) {
   size_t off = kWsHeader;
   L.align_scratch = off; off = align_up(off + align_scratch_bytes(num_pairs, E), 256);
   L.sorted_ids = off; off = align_up(off + static_cast<size_t>(L.cap) * 4, 256);
+  L.sorted_tok = off; off = align_up(off + static_cast<size_t>(L.cap) * 4, 256);
   L.expert_ids = off; off = align_up(off + static_cast<size_t>(L.cap / block_m + 1) * 4, 256);
   L.expert_offsets = off; off = align_up(off + static_cast<size_t>(E + 1) * 4, 256);
   L.ntpp = off; off = align_up(off + 4, 1024);
@@ -153,6 +161,7 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   uint8_t* w = static_cast<uint8_t*>(ws);
   int* err = reinterpret_cast<int*>(w);
   int32_t* sorted_ids = reinterpret_cast<int32_t*>(w + L.sorted_ids);
+  int32_t* sorted_tok = reinterpret_cast<int32_t*>(w + L.sorted_tok);
   int32_t* expert_ids = reinterpret_cast<int32_t*>(w + L.expert_ids);
   int32_t* offsets = reinterpret_cast<int32_t*>(w + L.expert_offsets);
   int32_t* ntpp = reinterpret_cast<int32_t*>(w + L.ntpp);
@@ -167,7 +176,7 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   if (st != MOE_OK) return st;
   stage_mark(1, s);
   st = launch_align(topk_ids, num_pairs, E, plan.block_m, sorted_ids, expert_ids, offsets, ntpp, w + L.align_scratch,
-                    err, s);
+                    err, s, sorted_tok, topk);
   if (st != MOE_OK) return st;
   stage_mark(2, s);
   const size_t n4 = static_cast<size_t>(T) * H / 4;
@@ -175,9 +184,13 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   if (plan.swap)
     st = launch_swap_gate_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_gate_up),
                              sorted_ids, offsets, h, err, num_pairs, topk, H, I, E, plan.nmax, s);
+  else if (plan.pair_gate_up && gate_up_pair2_supported(I))
+    st = launch_gemm_gate_up_pair2(static_cast<const __nv_bfloat16*>(x),
+                                   static_cast<const __nv_bfloat16*>(w_gate_up), sorted_tok, offsets, h, err,
+                                   num_pairs, topk, H, I, E, s);
   else
     st = launch_gemm_gate_up_pairs(static_cast<const __nv_bfloat16*>(x),
-                                   static_cast<const __nv_bfloat16*>(w_gate_up), sorted_ids, offsets, h, err,
+                                   static_cast<const __nv_bfloat16*>(w_gate_up), sorted_tok, offsets, h, err,
                                    num_pairs, topk, H, I, E, s);
   if (st != MOE_OK) return st;
   stage_mark(4, s);

@@ -1,11 +1,12 @@
 // gate_up grouped GEMM on row-block pairs of the expert-sorted layout.
 //
 // Follows the mini-sglang MoE chapter ("fused MoE", fused_moe_kernel and
-// FusedMoeBackend.forward) like the 128-row kernel in gemm_sorted.cu: rows are
-// the pairs sorted_token_ids[...] of one expert, gathered from X in-kernel
-// (pair / topk), C = X_rows @ W1[e]^T with the gate tile [n0, n0+128) stacked
-// over the up tile [I+n0, I+n0+128), and the epilogue writes h = silu(gate)*up
-// (the chapter's third exercise).
+// FusedMoeBackend.forward): rows are the pairs sorted_token_ids[...] of one
+// expert, gathered from X in-kernel (row pair / topk, read from the token
+// table that the align step writes beside sorted_token_ids),
+// C = X_rows @ W1[e]^T with the gate tile [n0, n0+128) stacked over the up
+// tile [I+n0, I+n0+128), and the epilogue writes h = silu(gate)*up (the
+// chapter's third exercise).
 //
 // Here a tile is up to two consecutive 128-row blocks of one expert (256 rows)
 // x 256 accumulator columns: both row halves multiply the same staged weight
@@ -16,12 +17,15 @@
 // short next to the main loop). An expert with an odd number of blocks ends
 // with a one-block tile.
 //
-// Kernel shape (one persistent CTA per SM, 352 threads): warps 0-3 epilogue
-// (both row halves, TMEM lane quarter = warp), warps 4-9 producers (warps 4+2s
-// and 5+2s own ring slot s and gather its two row halves with cp.async; warp
-// 4+2s's lane 0 also sends the weight tile by TMA), warp 10 owns TMEM and
-// issues the MMAs. The per-expert pair counts are prefix-summed in shared
-// memory from expert_offsets at kernel start.
+// Kernel shape (one persistent CTA per SM, 384 threads): warps 0-3 epilogue
+// (both row halves, TMEM lane quarter = warp), warp 4 sends the weight tile of
+// every ring slot by TMA, warps 5-10 gather (warps 5+2s and 6+2s own the two row
+// halves of ring slot s), warp 11 owns TMEM and issues the MMAs. A gather lane
+// keeps the source offsets of its 32 rows of the tile in registers, so that its
+// cp.async instructions issue back to back (reading each offset from shared
+// memory between them made the gather issue-bound), and no gather lane waits
+// for a TMA issue. The per-expert pair counts are prefix-summed in shared memory
+// from expert_offsets at kernel start.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -41,27 +45,24 @@ constexpr int kHalfBytes = kHalf * kBK * 2;
 constexpr int kABytes = 2 * kHalfBytes;
 constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kEpiWarps = 4;
-constexpr int kProdWarps = 2 * kStages;
-constexpr int kMmaWarp = kEpiWarps + kProdWarps;
+constexpr int kTmaWarp = kEpiWarps;
+constexpr int kGatherWarp0 = kEpiWarps + 1;
+constexpr int kMmaWarp = kGatherWarp0 + 2 * kStages;
 constexpr int kGemmThreads = 32 * (kMmaWarp + 1);
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kStagePitch = 36;
-constexpr size_t kCtlBytes = 256 + 4 * (MOE_MAX_EXPERTS + 1) + 12 + kProdWarps * kHalf * 4 + kEpiWarps * 32 * kStagePitch * 4;
+constexpr size_t kCtlBytes = 256 + 4 * (MOE_MAX_EXPERTS + 1) + 12 + kEpiWarps * 32 * kStagePitch * 4;
 constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + kCtlBytes;
-
-enum GemmMode { kGateUp = 0, kDown = 1 };  // only kGateUp is launched
 
 struct GemmArgs {
   const __nv_bfloat16* x;
-  const int32_t* sorted_ids;
+  const int32_t* sorted_tok;  // token of each sorted row, -1 for padding
   const int32_t* offsets;
-  const float* topk_w;
   __nv_bfloat16* h;
-  float* y_acc;
   int* err;
-  int num_pairs, topk, E;
+  int E;
   int K;
-  int I, H;
+  int I;
   int n_tiles;
   int b_rows_per_expert;
 };
@@ -92,10 +93,8 @@ __device__ __forceinline__ TileInfo decode_tile(const int* pfx, const int32_t* _
   return ti;
 }
 
-template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                    const GemmArgs args) {
+    moe_gate_up_kernel(const __grid_constant__ CUtensorMap map_b, const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -112,8 +111,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 132);
   int* pfx = reinterpret_cast<int*>(ctl + 256);
-  int* rowtabs = pfx + (MOE_MAX_EXPERTS + 1) + 3;
-  float* stg_all = reinterpret_cast<float*>(rowtabs + kProdWarps * kHalf);
+  float* stg_all = reinterpret_cast<float*>(pfx + (MOE_MAX_EXPERTS + 1) + 3);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -121,7 +119,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(full_bar(s), MODE == kGateUp ? 2 * 32 + 1 : 1);
+      ptx::mbar_init(full_bar(s), 3);  // weight expect_tx arrive + one arrive per gather warp
       ptx::mbar_init(empty_bar(s), 1);
     }
     ptx::mbar_init(tfull_bar, 1);
@@ -160,9 +158,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     if (lane == 31) pfx[args.E] = incl;
-  } else if (warp == kEpiWarps) {
+  } else if (warp == kTmaWarp) {
     ptx::prefetch_tmap(&map_b);
-    if (MODE == kDown) ptx::prefetch_tmap(&map_a);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -172,89 +169,85 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int tiles = pfx[args.E] * args.n_tiles;
   const int kblocks = args.K / kBK;
 
-  if (warp >= kEpiWarps && warp < kMmaWarp) {
-    const int pw = warp - kEpiWarps;
-    if (MODE == kGateUp) {
-      const int slot = pw >> 1;
-      const int half = pw & 1;
-      int* rowtab = rowtabs + pw * kHalf;
-      int cached_t = -1, fills = 0;
-      TileInfo ti{0, 0, 0, 0};
-      const uint32_t a_dst = sA + slot * kABytes + half * kHalfBytes;
-      const uint32_t b_dst = sB + slot * kBBytes;
-      const int chunk = lane & 7;
-      const int rsub = lane >> 3;
-      for (int g = slot;; g += kStages) {
-        const int t_local = g / kblocks;
-        const int t = blockIdx.x + t_local * gridDim.x;
-        if (t >= tiles) break;
-        const int kb = g - t_local * kblocks;
-        if (t != cached_t) {
-          ti = decode_tile(pfx, args.offsets, args.E, args.n_tiles, t);
-          const bool present = half < ti.nblk;
-#pragma unroll
-          for (int q = 0; q < kHalf / 32; ++q) {
-            int off = -1;
-            if (present) {
-              const int sid = __ldg(args.sorted_ids + ti.row0 + half * kHalf + q * 32 + lane);
-              off = (sid < args.num_pairs) ? (sid / args.topk) * args.K : -1;
-            }
-            rowtab[q * 32 + lane] = off;
-          }
-          cached_t = t;
-          __syncwarp();
-        }
-        const uint32_t use = static_cast<uint32_t>(g / kStages);
-        if (!ptx::mbar_wait(empty_bar(slot), (use & 1u) ^ 1u, abort_flag)) break;
-        if (half == 0 && lane == 0) {
-          const int b_row0 = ti.e * args.b_rows_per_expert + ti.nt * kHalf;
-          ptx::mbar_arrive_expect_tx(full_bar(slot), kBBytes);
-          ptx::tma_load_2d(b_dst, &map_b, full_bar(slot), kb * kBK, b_row0);
-          ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(slot), kb * kBK, b_row0 + args.I);
-          ++fills;
-        }
-        if (half < ti.nblk) {
-          const int k0 = kb * kBK + chunk * 8;
-#pragma unroll 8
-          for (int i = 0; i < kHalf / 4; ++i) {
-            const int r = i * 4 + rsub;
-            const int off = rowtab[r];
-            const uint32_t dst = a_dst + r * 128 + ((chunk ^ (r & 7)) << 4);
-            ptx::cp_async_16(dst, off >= 0 ? args.x + off + k0 : args.x, off >= 0 ? 16u : 0u);
-          }
-          ptx::cp_async_commit();
-          ptx::cp_async_wait<0>();
-          ptx::fence_proxy_async_smem();
-        }
-        ptx::mbar_arrive(full_bar(slot));
-      }
-      ptx::cp_async_wait<0>();
-      if (half == 0 && lane == 0 && fills > 0) ptx::mbar_wait_drain(full_bar(slot), (fills - 1) & 1);
-    } else if (pw == 0 && lane == 0) {
-      int stage = 0;
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      int stage = 0, issued = 0;
       uint32_t phase = 0;
-      int fills[kStages] = {0, 0, 0};
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile(pfx, args.offsets, args.E, args.n_tiles, t);
-        const int b_row0 = ti.e * args.b_rows_per_expert + ti.nt * kBN;
+        const int b_row0 = ti.e * args.b_rows_per_expert + ti.nt * kHalf;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
-          const uint32_t a_dst = sA + stage * kABytes;
           const uint32_t b_dst = sB + stage * kBBytes;
-          ptx::mbar_arrive_expect_tx(full_bar(stage), kBBytes + ti.nblk * kHalfBytes);
+          ptx::mbar_arrive_expect_tx(full_bar(stage), kBBytes);
           ptx::tma_load_2d(b_dst, &map_b, full_bar(stage), kb * kBK, b_row0);
-          ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(stage), kb * kBK, b_row0 + kHalf);
-          ptx::tma_load_2d(a_dst, &map_a, full_bar(stage), kb * kBK, ti.row0);
-          if (ti.nblk == 2)
-            ptx::tma_load_2d(a_dst + kHalfBytes, &map_a, full_bar(stage), kb * kBK, ti.row0 + kHalf);
-          ++fills[stage];
+          ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(stage), kb * kBK, b_row0 + args.I);
+          ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
-      for (int st = 0; st < kStages; ++st)
-        if (fills[st] > 0) ptx::mbar_wait_drain(full_bar(st), (fills[st] - 1) & 1);
+#pragma unroll
+      for (int st = 0; st < kStages; ++st) {
+        const int fills = issued / kStages + (st < issued % kStages ? 1 : 0);
+        if (fills > 0) ptx::mbar_wait_drain(full_bar(st), (fills - 1) & 1);
+      }
     }
+    __syncwarp();
+  } else if (warp >= kGatherWarp0 && warp < kMmaWarp) {
+    const int pw = warp - kGatherWarp0;
+    const int slot = pw >> 1;
+    const int half = pw & 1;
+    const uint32_t a_dst = sA + slot * kABytes + half * kHalfBytes;
+    const int chunk = lane & 7;
+    const int rsub = lane >> 3;
+    const __nv_bfloat16* xc = args.x + chunk * 8;
+    // Token rows 4i + rsub of the half: offs holds the current tile's source
+    // offsets, pre the next tile's tokens, loaded while this tile streams.
+    int offs[kHalf / 4], pre[kHalf / 4];
+    int cached_t = -1, pre_t = -1;
+    bool present = false, pre_present = false;
+    auto load_toks = [&](int tt) {
+      const TileInfo tj = decode_tile(pfx, args.offsets, args.E, args.n_tiles, tt);
+      pre_present = half < tj.nblk;
+      const int32_t* toks = args.sorted_tok + tj.row0 + half * kHalf + rsub;
+#pragma unroll
+      for (int i = 0; i < kHalf / 4; ++i) pre[i] = pre_present ? __ldg(toks + 4 * i) : -1;
+      pre_t = tt;
+    };
+    for (int g = slot;; g += kStages) {
+      const int t_local = g / kblocks;
+      const int t = blockIdx.x + t_local * gridDim.x;
+      if (t >= tiles) break;
+      const int kb = g - t_local * kblocks;
+      if (t != cached_t) {
+        if (pre_t != t) load_toks(t);
+        present = pre_present;
+#pragma unroll
+        for (int i = 0; i < kHalf / 4; ++i) offs[i] = pre[i] >= 0 ? pre[i] * args.K : -1;
+        cached_t = t;
+        if (t + static_cast<int>(gridDim.x) < tiles) load_toks(t + gridDim.x);
+      }
+      const uint32_t use = static_cast<uint32_t>(g / kStages);
+      const bool ok = ptx::mbar_wait(empty_bar(slot), (use & 1u) ^ 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      if (present) {
+        const int k0 = kb * kBK;
+#pragma unroll
+        for (int i = 0; i < kHalf / 4; ++i) {
+          const int r = i * 4 + rsub;
+          const int off = offs[i];
+          const uint32_t dst = a_dst + r * 128 + ((chunk ^ (r & 7)) << 4);
+          ptx::cp_async_16(dst, off >= 0 ? xc + off + k0 : args.x, off >= 0 ? 16u : 0u);
+        }
+        ptx::cp_async_commit();
+        ptx::cp_async_wait<0>();
+        ptx::fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(full_bar(slot));
+    }
+    ptx::cp_async_wait<0>();
   } else if (warp == kMmaWarp) {
     if (ptx::elect_one()) {
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(kHalf, kBN);
@@ -294,64 +287,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const TileInfo ti = decode_tile(pfx, args.offsets, args.E, args.n_tiles, t);
       if (!ptx::mbar_wait(tfull_bar, static_cast<uint32_t>(it) & 1u, abort_flag)) break;
       ptx::tc_fence_after();
+      const int n0 = ti.nt * kHalf;
       for (int half = 0; half < ti.nblk; ++half) {
         const uint32_t tbase = tmem_base + lane_off + half * kBN;
         const int rowbase = ti.row0 + half * kHalf + warp * 32;
-        if (MODE == kGateUp) {
-          const int n0 = ti.nt * kHalf;
 #pragma unroll 1
-          for (int c = 0; c < kHalf / 32; ++c) {
-            uint32_t g[32], u[32];
-            ptx::tmem_ld32(tbase + c * 32, g);
-            ptx::tmem_ld32(tbase + kHalf + c * 32, u);
-            ptx::tmem_ld_wait();
-            uint32_t* srow = reinterpret_cast<uint32_t*>(stg + lane * kStagePitch);
+        for (int c = 0; c < kHalf / 32; ++c) {
+          uint32_t g[32], u[32];
+          ptx::tmem_ld32(tbase + c * 32, g);
+          ptx::tmem_ld32(tbase + kHalf + c * 32, u);
+          ptx::tmem_ld_wait();
+          uint32_t* srow = reinterpret_cast<uint32_t*>(stg + lane * kStagePitch);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-              const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
-              const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
-              srow[j] = *reinterpret_cast<const uint32_t*>(&hv);
-            }
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int rl = i * 4 + (lane >> 3);
-              const int q = lane & 7;
-              const uint32_t* src = reinterpret_cast<const uint32_t*>(stg + rl * kStagePitch) + 2 * q;
-              uint2* dst = reinterpret_cast<uint2*>(args.h + static_cast<size_t>(rowbase + rl) * args.I + n0 + c * 32) + q;
-              *dst = make_uint2(src[0], src[1]);
-            }
-            __syncwarp();
+          for (int j = 0; j < 16; ++j) {
+            const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+            const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
+            srow[j] = *reinterpret_cast<const uint32_t*>(&hv);
           }
-        } else {
-          const int sid = __ldg(args.sorted_ids + rowbase + lane);
-          const bool valid = sid < args.num_pairs;
-          const float w = valid ? __ldg(args.topk_w + sid) : 0.f;
-          const int tok = valid ? sid / args.topk : -1;
-#pragma unroll 1
-          for (int c = 0; c < kBN / 32; ++c) {
-            uint32_t d[32];
-            ptx::tmem_ld32(tbase + c * 32, d);
-            ptx::tmem_ld_wait();
-            float4* srow = reinterpret_cast<float4*>(stg + lane * kStagePitch);
+          __syncwarp();
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              srow[q] = make_float4(w * __uint_as_float(d[4 * q]), w * __uint_as_float(d[4 * q + 1]),
-                                    w * __uint_as_float(d[4 * q + 2]), w * __uint_as_float(d[4 * q + 3]));
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int rl = i * 4 + (lane >> 3);
-              const int q = lane & 7;
-              const int trow = __shfl_sync(0xffffffffu, tok, rl);
-              const float4 v = reinterpret_cast<const float4*>(stg + rl * kStagePitch)[q];
-              if (trow >= 0)
-                atomicAdd(reinterpret_cast<float4*>(args.y_acc + static_cast<size_t>(trow) * args.H + ti.nt * kBN +
-                                                    c * 32) + q, v);
-            }
-            __syncwarp();
+          for (int i = 0; i < 8; ++i) {
+            const int rl = i * 4 + (lane >> 3);
+            const int q = lane & 7;
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(stg + rl * kStagePitch) + 2 * q;
+            uint2* dst =
+                reinterpret_cast<uint2*>(args.h + static_cast<size_t>(rowbase + rl) * args.I + n0 + c * 32) + q;
+            *dst = make_uint2(src[0], src[1]);
           }
+          __syncwarp();
         }
       }
       ptx::tc_fence_before();
@@ -368,19 +332,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 }  // namespace pair
 
-moe_status_t launch_gemm_gate_up_pairs(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_ids,
+moe_status_t launch_gemm_gate_up_pairs(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_tok,
                                        const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
                                        int H, int I, int E, cudaStream_t s) {
+  (void)num_pairs; (void)topk;
   using namespace pair;
   CUtensorMap map_b;
   if (!make_tmap_bf16_2d(&map_b, w1, static_cast<uint64_t>(E) * 2 * I, H)) return MOE_ERR_CUDA;
   GemmArgs a{};
-  a.x = x; a.sorted_ids = sorted_ids; a.offsets = offsets; a.h = h; a.err = err;
-  a.num_pairs = num_pairs; a.topk = topk; a.E = E; a.K = H; a.I = I; a.H = H;
+  a.x = x; a.sorted_tok = sorted_tok; a.offsets = offsets; a.h = h; a.err = err;
+  a.E = E; a.K = H; a.I = I;
   a.n_tiles = I / kHalf; a.b_rows_per_expert = 2 * I;
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_gemm_kernel<kGateUp>), static_cast<int>(kGemmSmem)))
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_gate_up_kernel), static_cast<int>(kGemmSmem)))
     return MOE_ERR_CUDA;
-  moe_gemm_kernel<kGateUp><<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_b, map_b, a);
+  moe_gate_up_kernel<<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_b, a);
   return launch_status();
 }
 
