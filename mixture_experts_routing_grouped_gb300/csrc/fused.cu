@@ -33,6 +33,11 @@ bool gate_up_pair2_supported(int I);
 moe_status_t launch_gemm_gate_up_pair2(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_tok,
                                        const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
                                        int H, int I, int E, cudaStream_t s);
+bool down_pair2_supported(int H, int I);
+moe_status_t launch_gemm_down_pair2(const __nv_bfloat16* h, const __nv_bfloat16* w2, const int32_t* sorted_ids,
+                                    const int32_t* sorted_tok, const int32_t* offsets, const float* topk_w,
+                                    float* y_acc, int* err, int num_pairs, int cap, int H, int I, int E,
+                                    cudaStream_t s);
 moe_status_t launch_gemm_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, const int32_t* sorted_ids,
                               const int32_t* expert_ids, const int32_t* ntpp, const float* topk_w, float* y_acc,
                               int* err, int num_pairs, int topk, int cap, int H, int I, int E, cudaStream_t s);
@@ -50,11 +55,15 @@ namespace {
 // use the swap-AB kernels with 16-row blocks and token tiles of <= 32; larger
 // ones use the sorted-layout kernels with 128-row blocks. The
 // MOE_GB300_PREFILL_KERNEL environment variable selects another large-problem
-// kernel for comparisons on one workload: "swap" (token tiles of <= 256 on
-// 16-row blocks) or "cta_pair" (gate_up on CTA pairs, I a multiple of 256).
+// kernels for comparisons on one workload: "swap" (token tiles of <= 256 on
+// 16-row blocks) or "cta_pair" (both grouped GEMMs on CTA pairs, cta_group::2;
+// gate_up needs I a multiple of 256). The CTA-pair kernels halve what each SM
+// loads per K step but compute an expert's odd last block as a full 256-row
+// tile; at the prefill shape the one-SM kernels are slightly faster.
 struct Plan {
   bool swap;
   bool pair_gate_up;
+  bool pair_down;
   int nmax;
   int block_m;
 };
@@ -70,7 +79,7 @@ Plan choose_plan(int T, int E, int topk) {
       p.swap = true; p.nmax = 256; p.block_m = 16;
     } else {
       p.swap = false; p.nmax = 0; p.block_m = 128;
-      p.pair_gate_up = env && std::strcmp(env, "cta_pair") == 0;
+      p.pair_gate_up = p.pair_down = env && std::strcmp(env, "cta_pair") == 0;
     }
   }
   return p;
@@ -197,6 +206,9 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   if (plan.swap)
     st = launch_swap_down(h, static_cast<const __nv_bfloat16*>(w_down), sorted_ids, offsets, topk_weights, y_acc, err,
                           num_pairs, topk, L.cap, H, I, E, plan.nmax, s);
+  else if (plan.pair_down && down_pair2_supported(H, I))
+    st = launch_gemm_down_pair2(h, static_cast<const __nv_bfloat16*>(w_down), sorted_ids, sorted_tok, offsets,
+                                topk_weights, y_acc, err, num_pairs, L.cap, H, I, E, s);
   else
     st = launch_gemm_down(h, static_cast<const __nv_bfloat16*>(w_down), sorted_ids, expert_ids, ntpp, topk_weights,
                           y_acc, err, num_pairs, topk, L.cap, H, I, E, s);

@@ -29,11 +29,13 @@
 // its row offset made the gather issue-bound), and no gather lane ever waits for
 // a TMA issue.
 //
-// Cross-CTA protocol (all waits bounded):
+// Cross-CTA protocol (all waits bounded). Barrier operations are CTA-scope
+// except where the odd CTA's gathered rows (generic-proxy writes to its own
+// shared memory, read by the even CTA's MMA) are published: that arrive is a
+// cluster-scope release and the MMA's wait on full[s] a cluster-scope acquire.
+// Cluster-scope operations on every ring step cost several times the step.
 //   full[s]  (even CTA, 4 arrivals): per CTA one arrive.expect_tx of its weight
-//            bytes (completed by its TMA loads) and one arrive after its gather
-//            (the even CTA's own arrivals are CTA-scope, the odd CTA's are
-//            cluster-scope releases on the even CTA's barrier);
+//            bytes (completed by its TMA loads) and one arrive after its gather;
 //   empty[s] (both CTAs): one multicast commit after the MMAs of the slot;
 //   tfull    (both CTAs): one multicast commit after the last K step of a tile;
 //   tempty   (even CTA, 8 arrivals): one per epilogue warp of either CTA.
@@ -196,13 +198,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileInfo ti = decode_tile(pfx, args.offsets, args.E, args.n_tiles, t);
       const int b_row0 = ti.e * 2 * args.I + ti.nt * kBN + static_cast<int>(rank) * kHalfN;
       for (int kb = 0; kb < kblocks; ++kb) {
-        const bool w = ptx::mbar_wait_cluster(empty_bar(stage), phase ^ 1u, abort_flag);
+        const bool w = ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         if (lane == 0) {
           const uint32_t b_dst = sB + stage * kBBytes;
           const uint32_t full_c = ptx::mapa_shared(full_bar(stage), 0);
-          if (rank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), kBBytes);
-          else ptx::mbar_arrive_expect_tx_cluster(full_c, kBBytes);
+          ptx::mbar_arrive_expect_tx_remote(full_c, kBBytes);
           ptx::tma_load_2d_pair(b_dst, &map_b, full_c, kb * kBK, b_row0);
           ptx::tma_load_2d_pair(b_dst + kBHalfBytes, &map_b, full_c, kb * kBK, b_row0 + args.I);
         }
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t + ncl < tiles) load_toks(t + ncl);
       }
       const uint32_t use = static_cast<uint32_t>(g / kStages);
-      const bool ok = ptx::mbar_wait_cluster(empty_bar(slot), (use & 1u) ^ 1u, abort_flag);
+      const bool ok = ptx::mbar_wait(empty_bar(slot), (use & 1u) ^ 1u, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       if (present) {
         const int k0 = kb * kBK;
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int t = cid; t < tiles && ok; t += ncl, ++it) {
-        if (!ptx::mbar_wait_cluster(tempty_bar, (static_cast<uint32_t>(it) & 1u) ^ 1u, abort_flag)) break;
+        if (!ptx::mbar_wait(tempty_bar, (static_cast<uint32_t>(it) & 1u) ^ 1u, abort_flag)) break;
         ptx::tc_fence_after();
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait_cluster(full_bar(stage), phase, abort_flag)) { ok = false; break; }
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     for (int t = cid; t < tiles; t += ncl, ++it) {
       const TileInfo ti = decode_tile(pfx, args.offsets, args.E, args.n_tiles, t);
-      const bool ok = ptx::mbar_wait_cluster(tfull_bar, static_cast<uint32_t>(it) & 1u, abort_flag);
+      const bool ok = ptx::mbar_wait(tfull_bar, static_cast<uint32_t>(it) & 1u, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
       if (static_cast<int>(rank) < ti.nblk) {
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(tempty_c);
+      if (lane == 0) ptx::mbar_arrive_remote(tempty_c);
     }
   }
 

@@ -138,6 +138,17 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
+// Arrive on an mbarrier that may sit in the peer CTA (shared::cluster address),
+// with the default CTA-scope release: enough where the arrive orders nothing
+// but tensor-memory reads fenced by tcgen05.fence and byte counts of TMA loads
+// (whose data the barrier's completion itself publishes). Cluster-scope
+// release/acquire on every ring step costs several times the step.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cbar), "r"(bytes) : "memory");
+}
 // Arrive on an mbarrier anywhere in the cluster (shared::cluster address).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
