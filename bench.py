@@ -160,7 +160,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
     y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
     tw = torch.empty((cfg.T, cfg.topk), dtype=torch.float32, device=dev)
     ids = torch.empty((cfg.T, cfg.topk), dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
 
     def step(x, g, yy, w_, i_):
         moe.moe_fused_forward(x, g, W["w1"], W["w2"], cfg.topk, cfg.renormalize, cfg.num_expert_group,
@@ -185,7 +185,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     for k in range(K):
-        flush.fill_(float(k))
+        flush(k)
         moe.moe_set_stage_events(ev[k])
         step(acts["x"], acts["gating"], y, tw, ids)
         moe.moe_set_stage_events(None)
@@ -215,7 +215,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
     xd, gd = torch.empty_like(acts["x"]), torch.empty_like(acts["gating"])
     e2e = []
     for k in range(args.warmup + K):
-        flush.fill_(float(k))
+        flush(k)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         xd.copy_(xh, non_blocking=True)
@@ -259,7 +259,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
         "dtype": "bf16",
         "data": "synthetic (seeded counter-based normal inputs, random-init expert weights)",
         "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "topk": cfg.topk,
-                   "routing": "softmax, renormalize, G=1", "l2": "256 MiB flush write between timed steps",
+                   "routing": "softmax, renormalize, G=1", "l2": "between timed steps: 256 MiB write then 256 MiB read (L2 is 129 MB; the read leaves no dirty lines to write back inside a timed step)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"kernel": "pair::moe_gemm_kernel<gate_up>", "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
@@ -279,6 +279,28 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
         result["gmm_lowp"] = bench_lowp(moe, synth, torch, dev, flush, peaks, args)
     del W
     return result, cfg
+
+
+class L2Flush:
+    """Untimed work between timed steps: write a 256 MiB buffer (more than the
+    129 MB L2), then read another 256 MiB buffer so that the dirty lines of the
+    write are written back now and not inside the timed step, then keep the GPU
+    busy (~0.1 ms) while the host enqueues the start event and the timed launches,
+    so that host-side call overhead (Python, ctypes, tensor-map encoding) never
+    shows up inside a device-timed interval."""
+
+    def __init__(self, torch, dev):
+        self.torch = torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+        self(0)  # the first reduction call sets up state that must not land in a timed step
+        torch.cuda.synchronize()
+
+    def __call__(self, k):
+        self.w.fill_(float(k))
+        self.torch.sum(self.r, dim=0, out=self.sink)
+        self.torch.cuda._sleep(200_000)
 
 
 def bench_decode(moe, synth, torch, dev, flush, peaks, args):
@@ -301,14 +323,14 @@ def bench_decode(moe, synth, torch, dev, flush, peaks, args):
         n_active = int(np.unique(ids.cpu().numpy()).size)
         times = []
         for k in range(max(5, args.steps)):
-            flush.fill_(float(k))
+            flush(k)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             run()
             b.record()
             b.synchronize()
             times.append(a.elapsed_time(b))
-        ms = statistics.mean(times)
+        ms = statistics.median(times)
         wbytes = n_active * 3 * cfg.I * cfg.H * 2
         gbs = wbytes / (ms * 1e-3) / 1e9
         out[f"T{T}"] = {"ms": round(ms, 4), "active_experts": n_active, "weight_bytes": wbytes,
@@ -332,14 +354,14 @@ def bench_routing(moe, synth, torch, dev, flush, peaks, args):
             run()
         times = []
         for k in range(max(10, args.steps)):
-            flush.fill_(float(k))
+            flush(k)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             run()
             b.record()
             b.synchronize()
             times.append(a.elapsed_time(b))
-        us = statistics.mean(times) * 1e3
+        us = statistics.median(times) * 1e3
         nbytes = T * cfg.E * 4 + T * cfg.topk * 8
         gbs = nbytes / (us * 1e-6) / 1e9
         out[f"T{T}"] = {"us": round(us, 2), "bytes": nbytes, "GB/s": round(gbs, 1),
@@ -367,7 +389,7 @@ def bench_lowp(moe, synth, torch, dev, flush, peaks, args):
             run()
         times = []
         for k in range(max(10, args.steps)):
-            flush.fill_(float(k))
+            flush(k)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             run()
@@ -376,7 +398,7 @@ def bench_lowp(moe, synth, torch, dev, flush, peaks, args):
             times.append(a.elapsed_time(b))
         if moe.moe_check_device_error(ws):
             raise RuntimeError("gmm_lowp reported a device error")
-        ms = statistics.mean(times)
+        ms = statistics.median(times)
         nbytes = n_active * cfg.N * cfg.K + cfg.M * cfg.K + cfg.M * cfg.N * 2 + cfg.M * 4 + cfg.E * cfg.N * 4
         gbs = nbytes / (ms * 1e-3) / 1e9
         tf = flops / (ms * 1e-3) / 1e12
@@ -461,7 +483,7 @@ def main():
         _b.build()
         peaks, _ = load_peaks()
         dev = torch.device("cuda", local_rank)
-        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        flush = L2Flush(torch, dev)
         fn = {"routing": bench_routing, "decode": bench_decode, "lowp": bench_lowp}[args.only]
         print(json.dumps({args.only: fn(moe, synth, torch, dev, flush, peaks, args)}), flush=True)
         return

@@ -13,11 +13,13 @@
 // group count) reduces the float logits directly; the generic kernel (any E and
 // G) reduces order-preserving unsigned keys of the logits.
 #include "common.cuh"
+#include "ptx.cuh"  // smem_u32
 
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
 namespace moe {
+
 namespace {
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -330,6 +332,273 @@ __global__ void __launch_bounds__(256) grouped_topk_kernel(const float* __restri
   zero_token_rows(zero, token, lane);
 }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Segmented kernel: L lanes per token (32 / L tokens per warp, 256 / L per CTA),
+// lane s of a token holding experts [s*P, (s+1)*P), and every real group of E/G
+// experts spanning L/G whole lanes. With one token per warp the k selection
+// rounds and the group ranking dominated the instruction count; here they are
+// L-lane segment reductions shared by 32 / L tokens.
+//
+// The CTA's logits (256 rows of P floats, one row per lane) are loaded with
+// coalesced 16-byte loads and stored to shared memory with the 16-byte chunk
+// bits of each address XORed with the address bits above the 128-byte line, so
+// that lanes reading chunk j of consecutive rows hit distinct banks. (Loading
+// each lane's own row directly touches 32 lines per warp instruction.)
+//
+// Phase 1 (3.2 / 3.3): row maxima, group maxima over the group's lanes, each
+// group's rank among the token's G groups. Phase 2 (3.4 / 3.5): the rows of the
+// selected groups are re-read from shared memory, F = G / topk_group lanes per
+// selected row and P / F values per lane, in increasing expert order across the
+// segment, so that every lane works on candidates; each lane caches its best two
+// (ties keep the lower expert index) and in each of the k rounds the segment
+// maximum and its lowest lane (ballot) give the next expert. A lane caches its
+// best four candidates (ties keep the lower expert index); only a lane that
+// wins a fifth time looks for its next candidate, in one pass for the best
+// value ranked below the one it just gave up. (Rebuilding a two-deep cache on a
+// third win was most of the instructions.) K > 0 fixes topk at compile time so
+// that the rounds unroll (K = 0: topk at run time).
+constexpr int kSegThreads = 128;  // a CTA holds 128 lane-rows: 128 / L tokens
+
+template <int P, int L, int F, int K>
+__global__ void __launch_bounds__(kSegThreads, 6) grouped_topk_seg_kernel(const float* __restrict__ gating, int T,
+                                                                          int G, int topk_group, int topk,
+                                                                          int scoring, int renorm, float rsf,
+                                                                          float* __restrict__ out_w,
+                                                                          int32_t* __restrict__ out_ids,
+                                                                          RouteZero zero) {
+  constexpr int kRowBytes = P * 4;
+  constexpr int kChunks = P / 4;  // 16-byte chunks per row, = chunks loaded per thread
+  constexpr int V = P / F;        // phase-2 values per lane
+  constexpr uint32_t kSwzMask = kRowBytes >= 32 ? kRowBytes / 16 - 1 : 0;
+  if (K > 0) topk = K;
+  __shared__ __align__(1024) uint8_t rows[kSegThreads * kRowBytes];
+  const int tid = threadIdx.x;
+  const uint32_t base = ptx::smem_u32(rows);
+  auto chunk_addr = [&](int row, int j) {  // shared address of 16-byte chunk j of lane-row `row`
+    uint32_t addr = static_cast<uint32_t>(row) * kRowBytes + j * 16;
+    return base + (addr ^ (((addr >> 7) & kSwzMask) << 4));
+  };
+  {
+    constexpr int E = P * L;
+    const size_t n4 = static_cast<size_t>(T) * E / 4;
+    const size_t first = static_cast<size_t>(blockIdx.x) * kSegThreads * kChunks;
+    const float4* src = reinterpret_cast<const float4*>(gating) + first;
+    float4 f[kChunks];
+#pragma unroll
+    for (int q = 0; q < kChunks; ++q) {
+      const int c = tid + kSegThreads * q;
+      f[q] = first + c < n4 ? __ldg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < kChunks; ++q) {
+      const int c = tid + kSegThreads * q;
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(chunk_addr(c / kChunks, c % kChunks)),
+                   "f"(f[q].x), "f"(f[q].y), "f"(f[q].z), "f"(f[q].w)
+                   : "memory");
+    }
+  }
+  __syncthreads();
+
+  const int lane = tid & 31;
+  const int s = lane & (L - 1);
+  const int seg0 = lane & ~(L - 1);
+  const int trow0 = tid - s;  // lane-row of the token's first lane in the CTA
+  const int token = static_cast<int>(blockIdx.x) * (kSegThreads / L) + tid / L;
+
+  // Phase 1: own row's maximum, group maximum, group rank.
+  float lm = -CUDART_INF_F;
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) {
+    float4 f;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                 : "r"(chunk_addr(tid, j))
+                 : "memory");
+    lm = max3f(lm, max3f(f.x, f.y, f.z), f.w);
+  }
+  const int lpg = L / G;
+  float gm = lm;
+  for (int o = 1; o < lpg; o <<= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+  bool selected = true;
+  if (topk_group < G) {
+    const int my_g = s / lpg;
+    int rank = 0;
+    for (int g = 0; g < G; ++g) {
+      const float o = __shfl_sync(0xffffffffu, gm, seg0 + g * lpg);
+      rank += (o > gm || (o == gm && g < my_g)) ? 1 : 0;
+    }
+    selected = rank < topk_group;
+  }
+  // Phase 2: lane s takes part s % F of the (s / F)-th selected row, in row order.
+  const uint32_t rowmask = (__ballot_sync(0xffffffffu, selected) >> seg0) & (L == 32 ? 0xffffffffu : ((1u << L) - 1u));
+  int my_row = s;
+  if (F > 1) {
+    uint32_t m = rowmask;
+    for (int i = 0; i < s / F; ++i) m &= m - 1;  // drop the lowest selected rows before ours
+    my_row = __ffs(m) - 1;
+  }
+  const bool has_row = F > 1 || selected;
+  const int part = s % F;
+  const int base_e = my_row * P + part * V;
+  float v[V];
+#pragma unroll
+  for (int j = 0; j < V / 4; ++j) {
+    float4 f;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                 : "r"(chunk_addr(trow0 + my_row, part * (V / 4) + j))
+                 : "memory");
+    v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+  }
+  // best four of the lane's candidates (b1 >= b2 >= b3 >= b4); indices ascend
+  // with j, so strict comparisons keep the lower index among equal values
+  float b1 = -CUDART_INF_F, b2 = -CUDART_INF_F, b3 = -CUDART_INF_F, b4 = -CUDART_INF_F;
+  int i1 = 0x7fffffff, i2 = 0x7fffffff, i3 = 0x7fffffff, i4 = 0x7fffffff;
+  if (has_row) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const float x = v[j];
+      const int ix = base_e + j;
+      const bool p1 = x > b1, p2 = x > b2, p3 = x > b3, p4 = x > b4;
+      b4 = p3 ? b3 : (p4 ? x : b4);
+      i4 = p3 ? i3 : (p4 ? ix : i4);
+      b3 = p2 ? b2 : (p3 ? x : b3);
+      i3 = p2 ? i2 : (p3 ? ix : i3);
+      b2 = p1 ? b1 : (p2 ? x : b2);
+      i2 = p1 ? i1 : (p2 ? ix : i2);
+      b1 = p1 ? x : b1;
+      i1 = p1 ? ix : i1;
+    }
+  }
+  float my_x = 0.f;
+  int my_id = 0;
+  const uint32_t segmask = L == 32 ? 0xffffffffu : (((1u << L) - 1u) << seg0);
+#pragma unroll(K > 0 ? K : 1)
+  for (int it = 0; it < topk; ++it) {
+    float m = b1;
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const uint32_t wm = __ballot_sync(0xffffffffu, b1 == m) & segmask;
+    const int wl = __ffs(wm) - 1;
+    const int wid = __shfl_sync(0xffffffffu, i1, wl & 31);
+    if (s == it) { my_x = m; my_id = wid; }
+    if (lane == wl) {
+      const float lv = b1;
+      const int li = i1;
+      b1 = b2; i1 = i2;
+      b2 = b3; i2 = i3;
+      b3 = b4; i3 = i4;
+      b4 = -CUDART_INF_F; i4 = 0x7fffffff;
+      if (b1 == -CUDART_INF_F) {
+        // cache exhausted: the best value ranked below (lv, li)
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+          const bool below = v[j] < lv || (v[j] == lv && base_e + j > li);
+          if (below && v[j] > b1) { b1 = v[j]; i1 = base_e + j; }
+        }
+      }
+    }
+  }
+
+  // 3.6: weights of the topk selections held by segment lanes 0..topk-1.
+  const bool active = s < topk;
+  float w;
+  if (scoring == MOE_SCORE_SOFTMAX) {
+    if (renorm) {
+      // softmax over the selected logits only: the full denominator cancels
+      const float x0 = __shfl_sync(0xffffffffu, my_x, seg0);
+      const float ex = active ? expf(my_x - x0) : 0.f;
+      float sum = ex;
+#pragma unroll
+      for (int o = 1; o < L; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      w = ex / sum;
+    } else {
+      float tm = lm;
+#pragma unroll
+      for (int o = 1; o < L; o <<= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+      float part_sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < kChunks; ++j) {
+        float4 f;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(f.x), "=f"(f.y), "=f"(f.z), "=f"(f.w)
+                     : "r"(chunk_addr(tid, j))
+                     : "memory");
+        part_sum += expf(f.x - tm) + expf(f.y - tm) + expf(f.z - tm) + expf(f.w - tm);
+      }
+#pragma unroll
+      for (int o = 1; o < L; o <<= 1) part_sum += __shfl_xor_sync(0xffffffffu, part_sum, o);
+      w = active ? expf(my_x - tm) / part_sum : 0.f;
+    }
+  } else {
+    const float sg = active ? 1.0f / (1.0f + expf(-my_x)) : 0.f;
+    w = sg;
+    if (renorm) {
+      float sum = sg;
+#pragma unroll
+      for (int o = 1; o < L; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      w = sg / sum;
+    }
+  }
+  w *= rsf;
+  if (token < T) {
+    if (active) {
+      out_w[static_cast<size_t>(token) * topk + s] = w;
+      out_ids[static_cast<size_t>(token) * topk + s] = my_id;
+    }
+    if (zero.rows) {
+      float4* r = zero.rows + static_cast<size_t>(token) * zero.row_f4;
+      for (int i = s; i < zero.row_f4; i += L) r[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (zero.cnt) {
+      int* c = zero.cnt + static_cast<size_t>(token) * zero.cnt_per_row;
+      for (int i = s; i < zero.cnt_per_row; i += L) c[i] = 0;
+    }
+  }
+}
+
+// Lanes per token for the segmented kernel (8, 16 or 32), or 0 when it does not
+// apply: P = E / L must be 4, 8, 16 or 32, every group must span whole lanes
+// (G divides L) and the topk results must fit one per lane (topk <= L).
+int seg_lanes(int E, int G, int k) {
+  for (int L = 8; L <= 32; L <<= 1) {
+    if (E % L != 0) continue;
+    const int P = E / L;
+    if ((P != 4 && P != 8 && P != 16 && P != 32) || L % G != 0 || k > L) continue;
+    return L;
+  }
+  return 0;
+}
+
+template <int P, int L, int F>
+void launch_seg_f(const float* gating, int T, int G, int kg, int k, int scoring, int renorm, float rsf, float* w,
+                  int32_t* ids, const RouteZero& z, cudaStream_t s) {
+  const int grid = cdiv(T, kSegThreads / L);
+  if (k == 8 && L >= 8)
+    grouped_topk_seg_kernel<P, L, F, 8><<<grid, kSegThreads, 0, s>>>(gating, T, G, kg, k, scoring, renorm, rsf, w,
+                                                                     ids, z);
+  else
+    grouped_topk_seg_kernel<P, L, F, 0><<<grid, kSegThreads, 0, s>>>(gating, T, G, kg, k, scoring, renorm, rsf, w,
+                                                                     ids, z);
+}
+
+template <int P, int L>
+moe_status_t launch_seg(const float* gating, int T, int G, int kg, int k, int scoring, int renorm, float rsf,
+                        float* w, int32_t* ids, const RouteZero& z, cudaStream_t s) {
+  // F = G / topk_group lanes share a selected row in phase 2 (1 when that is not
+  // 2 or 4, or leaves fewer than 4 values per lane)
+  const int F = (G % kg == 0) ? G / kg : 1;
+  if (F == 2 && P >= 8) launch_seg_f<P, L, 2>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  else if (F == 4 && P >= 16) launch_seg_f<P, L, 4>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  else launch_seg_f<P, L, 1>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  return launch_status();
+}
+
 template <int VPL>
 void launch_fast(const float* gating, int T, int G, int kg, int k, int scoring, int renorm, float rsf, float* w,
                  int32_t* ids, const RouteZero& z, cudaStream_t s) {
@@ -361,6 +630,28 @@ moe_status_t launch_grouped_topk(const float* gating, int T, int E, int G, int k
                                  int* zero_cnt, int cnt_per_row) {
   if (T == 0) return MOE_OK;
   const RouteZero z{reinterpret_cast<float4*>(zero_rows), zero_cols / 4, zero_cnt, cnt_per_row};
+  const int L = (G & (G - 1)) == 0 ? seg_lanes(E, G, k) : 0;
+  if (L == 8) {
+    switch (E / L) {
+      case 4: return launch_seg<4, 8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      case 8: return launch_seg<8, 8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      case 16: return launch_seg<16, 8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      case 32: return launch_seg<32, 8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      default: break;
+    }
+  } else if (L == 16) {
+    switch (E / L) {
+      case 16: return launch_seg<16, 16>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      case 32: return launch_seg<32, 16>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      default: break;
+    }
+  } else if (L == 32) {
+    switch (E / L) {
+      case 16: return launch_seg<16, 32>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      case 32: return launch_seg<32, 32>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      default: break;
+    }
+  }
   const bool pow2_groups = (G & (G - 1)) == 0;
   if (pow2_groups) {
     switch (E) {
