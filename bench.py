@@ -261,10 +261,10 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
         "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "I": cfg.I, "E": cfg.E, "topk": cfg.topk,
                    "routing": "softmax, renormalize, G=1", "l2": "between timed steps: 256 MiB write then 256 MiB read (L2 is 129 MB; the read leaves no dirty lines to write back inside a timed step)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "pair::moe_gemm_kernel<gate_up>", "bound": "tensor", "achieved": round(achieved, 1),
+        "roofline": {"kernel": "pair::moe_gate_up_kernel", "bound": "tensor", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"bf16_tflops (burst) of {peaks_kind}",
-                     "traffic": kernel_traffic("pair::moe_gemm_kernel<gate_up>")},
+                     "traffic": kernel_traffic("pair::moe_gate_up_kernel")},
         "layer_tflops": round(layer_tflops, 1),
         "layer_frac_bf16_peak": round(layer_tflops / peak, 4),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},

@@ -54,6 +54,10 @@ __global__ void __launch_bounds__(kAlignThreads)
   __shared__ int hist[MOE_MAX_EXPERTS];
   __shared__ int warp_tot[kAlignWarps];
   __shared__ int is_last;
+  // the last CTA reuses hist for the segment starts, and keeps counts and padded lengths
+  __shared__ int seg_count[MOE_MAX_EXPERTS];
+  __shared__ int seg_padded[MOE_MAX_EXPERTS];
+  int* seg_start = hist;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int e = tid; e < E; e += kAlignThreads) hist[e] = 0;
   __syncthreads();
@@ -73,10 +77,22 @@ __global__ void __launch_bounds__(kAlignThreads)
   if (!is_last) return;
   __threadfence();
 
-  // Last CTA: totals, padded segments, per-chunk bases. One expert per thread (E <= 1024).
+  // Last CTA: totals, padded segments, per-chunk bases. One expert per thread
+  // (E <= 1024) for the scans; the chunk histograms are read kBatch at a time
+  // before any of them is overwritten (a load of one slot after the store to the
+  // previous one would wait a full L2 round trip per chunk).
+  constexpr int kBatch = 16;
   int count = 0, padded = 0;
   if (tid < E) {
-    for (int c = 0; c < nchunks; ++c) count += __ldcg(chunk_base + static_cast<size_t>(c) * E + tid);
+    int c = 0;
+    for (; c + kBatch <= nchunks; c += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) v[j] = __ldcg(chunk_base + static_cast<size_t>(c + j) * E + tid);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) count += v[j];
+    }
+    for (; c < nchunks; ++c) count += __ldcg(chunk_base + static_cast<size_t>(c) * E + tid);
     padded = (count + block_m - 1) / block_m * block_m;
   }
   int incl = padded;
@@ -101,22 +117,41 @@ __global__ void __launch_bounds__(kAlignThreads)
   const int total = warp_tot[kAlignWarps - 1];
   if (tid < E) {
     expert_offsets[tid] = start;
+    seg_start[tid] = start;
+    seg_count[tid] = count;
+    seg_padded[tid] = padded;
     int run = start;
-    for (int c = 0; c < nchunks; ++c) {
+    int c = 0;
+    for (; c + kBatch <= nchunks; c += kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) v[j] = __ldcg(chunk_base + static_cast<size_t>(c + j) * E + tid);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        chunk_base[static_cast<size_t>(c + j) * E + tid] = run;
+        run += v[j];
+      }
+    }
+    for (; c < nchunks; ++c) {
       int32_t* slot = chunk_base + static_cast<size_t>(c) * E + tid;
       const int n = __ldcg(slot);
       *slot = run;
       run += n;
     }
-    for (int blk = start / block_m; blk < (start + padded) / block_m; ++blk) expert_ids[blk] = tid;
-    for (int pos = start + count; pos < start + padded; ++pos) {
-      sorted_ids[pos] = num_pairs;
-      if (sorted_tok) sorted_tok[pos] = -1;
-    }
   }
   if (tid == 0) {
     expert_offsets[E] = total;
     *ntpp = total;
+  }
+  __syncthreads();
+  // block experts and padding sentinels: one warp per expert
+  for (int e = warp; e < E; e += kAlignWarps) {
+    const int st = seg_start[e], cnt = seg_count[e], pd = seg_padded[e];
+    for (int blk = st / block_m + lane; blk < (st + pd) / block_m; blk += 32) expert_ids[blk] = e;
+    for (int pos = st + cnt + lane; pos < st + pd; pos += 32) {
+      sorted_ids[pos] = num_pairs;
+      if (sorted_tok) sorted_tok[pos] = -1;
+    }
   }
   for (int pos = total + tid; pos < cap; pos += kAlignThreads) {
     sorted_ids[pos] = num_pairs;
@@ -172,6 +207,142 @@ __global__ void __launch_bounds__(kAlignThreads)
   }
 }
 
+// Small problems (chunk histograms x experts <= kSmallScan): the count kernel
+// only writes each chunk's histogram, and every CTA of the scatter kernel reads
+// all of them (at most 256 KB from L2) and derives in shared memory the expert
+// totals, the padded segment starts and its own chunk's bases, so that no CTA
+// waits for a last one to finish the scan.
+constexpr int kSmallScan = 65536;
+
+__global__ void __launch_bounds__(kAlignThreads)
+    align_hist_kernel(const int32_t* __restrict__ ids, int num_pairs, int E, int chunk,
+                      int32_t* __restrict__ hists, int* __restrict__ err) {
+  __shared__ int hist[MOE_MAX_EXPERTS];
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += kAlignThreads) hist[e] = 0;
+  __syncthreads();
+  const int lo = blockIdx.x * chunk;
+  const int hi = min(num_pairs, lo + chunk);
+  for (int p = lo + tid; p < hi; p += kAlignThreads) {
+    const int e = __ldg(ids + p);
+    if (e < 0 || e >= E) report_error(err, MOE_DEVERR_EXPERT_ID);
+    else atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kAlignThreads) hists[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
+}
+
+__global__ void __launch_bounds__(kAlignThreads)
+    align_scan_scatter_kernel(const int32_t* __restrict__ ids, int num_pairs, int E, int block_m, int cap, int chunk,
+                              int nchunks, const int32_t* __restrict__ hists, int32_t* __restrict__ sorted_ids,
+                              int32_t* __restrict__ sorted_tok, int topk, int32_t* __restrict__ expert_ids,
+                              int32_t* __restrict__ expert_offsets, int32_t* __restrict__ ntpp) {
+  extern __shared__ int sm[];
+  int* cur = sm;                              // [kAlignWarps][E] write cursors
+  int* tot = cur + kAlignWarps * E;           // [E] pairs per expert
+  int* bef = tot + E;                         // [E] pairs of the expert in earlier chunks
+  int* seg = bef + E;                         // [E] padded segment starts
+  __shared__ int warp_tot[kAlignWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int i = tid; i < (kAlignWarps + 2) * E; i += kAlignThreads) sm[i] = 0;
+  __syncthreads();
+  const int n_h = nchunks * E;
+  for (int idx = tid; idx < n_h; idx += kAlignThreads) {
+    const int v = __ldcg(hists + idx);
+    if (v) {
+      const int c = idx / E, e = idx - c * E;
+      atomicAdd(&tot[e], v);
+      if (c < static_cast<int>(blockIdx.x)) atomicAdd(&bef[e], v);
+    }
+  }
+  __syncthreads();
+  // padded lengths -> exclusive scan over experts (one expert per thread, E <= 1024)
+  const int count = tid < E ? tot[tid] : 0;
+  const int padded = (count + block_m - 1) / block_m * block_m;
+  int incl = padded;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += n;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const int start = incl - padded + (warp > 0 ? warp_tot[warp - 1] : 0);
+  const int total = warp_tot[kAlignWarps - 1];
+  if (tid < E) seg[tid] = start;
+  if (blockIdx.x == 0) {
+    if (tid < E) expert_offsets[tid] = start;
+    if (tid == 0) {
+      expert_offsets[E] = total;
+      *ntpp = total;
+    }
+  }
+  __syncthreads();
+  // block experts and padding sentinels, spread over the grid (one SM alone is
+  // store-bound on them): one warp per expert, experts and tail strided by CTA
+  for (int e = static_cast<int>(blockIdx.x) * kAlignWarps + warp; e < E; e += nchunks * kAlignWarps) {
+    const int st = seg[e], cnt = tot[e];
+    const int pd = (cnt + block_m - 1) / block_m * block_m;
+    for (int blk = st / block_m + lane; blk < (st + pd) / block_m; blk += 32) expert_ids[blk] = e;
+    for (int pos = st + cnt + lane; pos < st + pd; pos += 32) {
+      sorted_ids[pos] = num_pairs;
+      if (sorted_tok) sorted_tok[pos] = -1;
+    }
+  }
+  const int g0 = static_cast<int>(blockIdx.x) * kAlignThreads + tid, gstride = nchunks * kAlignThreads;
+  for (int pos = total + g0; pos < cap; pos += gstride) {
+    sorted_ids[pos] = num_pairs;
+    if (sorted_tok) sorted_tok[pos] = -1;
+  }
+  for (int blk = total / block_m + g0; blk < cap / block_m; blk += gstride) expert_ids[blk] = -1;
+  // stable scatter of this chunk (as in align_scatter_kernel)
+  const int lo = blockIdx.x * chunk;
+  const int span = chunk / kAlignWarps;  // multiple of 32
+  const int wlo = min(num_pairs, lo + warp * span);
+  const int whi = min(num_pairs, wlo + span);
+  for (int b = wlo; b < whi; b += 32) {
+    const int p = b + lane;
+    const int v = (p < whi) ? __ldg(ids + p) : -1;
+    if (v >= 0 && v < E) atomicAdd(&cur[warp * E + v], 1);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kAlignThreads) {
+    int run = seg[e] + bef[e];
+    for (int w = 0; w < kAlignWarps; ++w) {
+      const int n = cur[w * E + e];
+      cur[w * E + e] = run;
+      run += n;
+    }
+  }
+  __syncthreads();
+  for (int b = wlo; b < whi; b += 32) {
+    const int p = b + lane;
+    int e = (p < whi) ? __ldg(ids + p) : -1;
+    if (e >= E) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int base = 0;
+    if (e >= 0) base = cur[warp * E + e];
+    __syncwarp();
+    if (e >= 0) {
+      sorted_ids[base + __popc(peers & lt_mask)] = p;
+      if (sorted_tok) sorted_tok[base + __popc(peers & lt_mask)] = p / topk;
+      if ((peers & lt_mask) == 0) cur[warp * E + e] = base + __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
 }  // namespace
 
 size_t align_max_padded(int num_pairs, int E, int block_m) {
@@ -195,6 +366,19 @@ moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m,
   const AlignPlan p = align_plan(num_pairs);
   int* done = static_cast<int*>(scratch);
   int32_t* chunk_base = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + 256);
+  if (p.nchunks * E <= kSmallScan) {
+    align_hist_kernel<<<p.nchunks, kAlignThreads, 0, s>>>(ids, num_pairs, E, p.chunk, chunk_base, err);
+    moe_status_t st = launch_status();
+    if (st != MOE_OK) return st;
+    const size_t smem = static_cast<size_t>(kAlignWarps + 3) * E * sizeof(int);
+    if (!ensure_smem_attr(reinterpret_cast<const void*>(align_scan_scatter_kernel),
+                          static_cast<int>(static_cast<size_t>(kAlignWarps + 3) * MOE_MAX_EXPERTS * sizeof(int))))
+      return MOE_ERR_CUDA;
+    align_scan_scatter_kernel<<<p.nchunks, kAlignThreads, smem, s>>>(
+        ids, num_pairs, E, block_m, cap, p.chunk, p.nchunks, chunk_base, sorted_ids, sorted_tok,
+        topk > 0 ? topk : 1, expert_ids, expert_offsets, ntpp);
+    return launch_status();
+  }
   align_count_scan_kernel<<<p.nchunks, kAlignThreads, 0, s>>>(ids, num_pairs, E, block_m, cap, p.chunk, p.nchunks,
                                                               chunk_base, done, sorted_ids, sorted_tok,
                                                               expert_ids, expert_offsets, ntpp, err);
