@@ -1,28 +1,23 @@
-// Grouped GEMMs of the MoE layer over the expert-sorted, BLOCK_M-padded pair
-// layout, on tcgen05 tensor cores with TMEM accumulators.
+// down grouped GEMM of the MoE layer over the expert-sorted, BLOCK_M-padded pair
+// layout, on tcgen05 tensor cores with TMEM accumulators, and the 2D tensor maps
+// (TMA descriptors) of the grouped GEMM kernels.
 //
 // Follows the mini-sglang MoE chapter ("fused MoE", fused_moe_kernel and
-// FusedMoeBackend.forward): every 128-row block of the sorted layout belongs to
-// one expert (expert_ids), its rows are the pairs sorted_token_ids[...], and
-//   gate_up pass: C[row] = X[pair / topk] @ W1[e]^T   (rows gathered in-kernel)
-//   down pass:    C[row] = h[row] @ W2[e]^T, scaled by the route weight and
-//                 summed into the pair's token row.
-// The SwiGLU of the chapter's third exercise is fused into the gate_up
-// epilogue: the B tile stacks 128 gate rows [n0, n0+128) over the matching 128
-// up rows [I+n0, I+n0+128), so each accumulator row holds the paired gate and
-// up columns and one thread writes h = silu(gate) * up directly. No
-// weight[topk_ids] and no permuted copy of X exist ("Fused MoE Part 3",
-// section 01): the gather happens while staging A into shared memory.
+// FusedMoeBackend.forward, second launch): every 128-row block of the sorted
+// layout belongs to one expert (expert_ids), its rows are the pairs
+// sorted_token_ids[...], and C[row] = h[row] @ W2[e]^T is scaled by the route
+// weight of the row's pair and summed into the pair's token row of the fp32
+// accumulator. h is contiguous per expert (the gate_up kernels write it in
+// sorted order), so both operands arrive by TMA.
 //
-// Kernel shape (one persistent CTA per SM, 288 threads):
-//   warps 0-3  epilogue: TMEM -> registers -> global (TMEM lane quarter = warp)
-//   warps 4-7  producers. gate_up: warp w owns ring slot w and stages every
-//              4th k-block (TMA for B, cp.async row gather for A), so four
-//              stages are in flight without any warp waiting on another's copies.
-//              down: one thread sends A and B by TMA through the 4-stage ring.
-//   warp 8     TMEM allocation and the single MMA-issuing thread
+// Kernel shape (one persistent CTA per SM, 192 threads):
+//   warps 0-3  epilogue: TMEM -> registers -> shared staging -> fp32 atomics
+//              (TMEM lane quarter = warp)
+//   warp 4     one thread sends A and B of every K step by TMA through the
+//              4-slot ring
+//   warp 5     TMEM allocation and the single MMA-issuing thread
 // The 128 x 256 fp32 accumulator lives in TMEM, double-buffered (512 columns)
-// so that the epilogue of one tile overlaps the main loop of the next.
+// so that the combine of one tile overlaps the main loop of the next.
 // Tiles (m-block, n-block) are taken round-robin with the n-block fastest, so
 // the CTAs working at one time share each expert's weight tiles through L2.
 #include "common.cuh"
@@ -41,40 +36,30 @@ constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;   // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;   // 32 KB
 constexpr int kEpiThreads = 128;
-constexpr int kProdThreads = 128;
+constexpr int kProdThreads = 32;
+constexpr int kMmaWarp = (kEpiThreads + kProdThreads) / 32;
 constexpr int kGemmThreads = kEpiThreads + kProdThreads + 32;
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kStagePitch = 36;  // floats per staged row (16-byte aligned, few bank conflicts)
 constexpr size_t kEpiStageBytes = 4 * 32 * kStagePitch * 4;
-constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 256 + 4 * kBM * 4 + kEpiStageBytes;
-static_assert(kStages == 4, "one producer warp per ring slot");
-
-enum GemmMode { kGateUp = 0, kDown = 1 };
+constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 256 + kEpiStageBytes;
 
 struct GemmArgs {
-  const __nv_bfloat16* x;         // gate_up: [T, H] activations gathered by row
   const int32_t* sorted_ids;      // [cap] pair index or sentinel num_pairs
   const int32_t* expert_ids;      // [cap / 128]
   const int32_t* ntpp;            // [1] padded rows in use
-  const float* topk_w;            // down: [num_pairs] route weights
-  __nv_bfloat16* h;               // gate_up out: [cap, I] in sorted order
-  float* y_acc;                   // down out: [T, H] fp32 accumulator
+  const float* topk_w;            // [num_pairs] route weights
+  float* y_acc;                   // [T, H] fp32 accumulator
   int* err;
   int num_pairs, topk;
-  int K;                          // reduction length (H, or I)
-  int I, H;
+  int K;                          // reduction length (I)
+  int H;
   int n_tiles;                    // n-blocks per m-block
-  int b_rows_per_expert;          // rows of the 2D weight view per expert (2I, or H)
+  int b_rows_per_expert;          // rows of the 2D weight view per expert (H)
 };
 
-// silu(g) = g / (1 + e^-g) with the fast reciprocal divide: its ~2-ulp error is
-// far below the bf16 rounding of h, and the IEEE divide sequence made the
-// epilogue slower than the main loop it overlaps.
-__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
-
-template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+    moe_down_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -100,7 +85,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(full_bar(s), MODE == kGateUp ? 32 + 1 : 1);
+      ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -111,13 +96,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
     ptx::tmem_relinquish();
   }
   if (tid == kEpiThreads) {
     ptx::prefetch_tmap(&map_b);
-    if (MODE == kDown) ptx::prefetch_tmap(&map_a);
+    ptx::prefetch_tmap(&map_a);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -128,68 +113,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int tiles = m_tiles * args.n_tiles;
   const int kblocks = args.K / kBK;
 
-  if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ producers
-    const int pw = warp - 4;
-    if (MODE == kGateUp) {
-      // Producer warp pw owns ring slot pw (kStages == 4 == producer warps) and
-      // stages every 4th k-block of this CTA's (tile, k-block) sequence: lane 0
-      // sends the B tile by TMA, the 32 lanes gather the 128 A rows with cp.async
-      // (16 B each, zero-fill for pad rows) into the 128B-swizzled layout, wait
-      // for their own copies, publish them to the async proxy and arrive.
-      int* rowtab = reinterpret_cast<int*>(ctl + 256) + pw * kBM;  // element offset of each row, -1 = pad
-      int cached_t = -1, e = 0, fills = 0;
-      const int slot = pw;
-      const uint32_t a_dst = sA + slot * kABytes;
-      const uint32_t b_dst = sB + slot * kBBytes;
-      const int chunk = lane & 7;
-      const int rsub = lane >> 3;
-      for (int g = pw;; g += kStages) {
-        const int t_local = g / kblocks;
-        const int t = blockIdx.x + t_local * gridDim.x;
-        if (t >= tiles) break;
-        const int kb = g - t_local * kblocks;
-        const int mt = t / args.n_tiles;
-        const int nt = t - mt * args.n_tiles;
-        if (t != cached_t) {
-#pragma unroll
-          for (int q = 0; q < kBM / 32; ++q) {
-            const int sid = __ldg(args.sorted_ids + mt * kBM + q * 32 + lane);
-            rowtab[q * 32 + lane] = (sid < args.num_pairs) ? (sid / args.topk) * args.K : -1;
-          }
-          e = __ldg(args.expert_ids + mt);
-          cached_t = t;
-          __syncwarp();
-        }
-        const uint32_t use = static_cast<uint32_t>(g / kStages);
-        if (!ptx::mbar_wait(empty_bar(slot), (use & 1u) ^ 1u, abort_flag)) break;
-        if (lane == 0) {
-          const int b_row0 = e * args.b_rows_per_expert + nt * kBM;
-          ptx::mbar_arrive_expect_tx(full_bar(slot), kBBytes);
-          ptx::tma_load_2d(b_dst, &map_b, full_bar(slot), kb * kBK, b_row0);
-          ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(slot), kb * kBK, b_row0 + args.I);
-          ++fills;
-        }
-        const int k0 = kb * kBK + chunk * 8;
-#pragma unroll 8
-        for (int i = 0; i < kBM / 4; ++i) {
-          const int r = i * 4 + rsub;
-          const int off = rowtab[r];
-          const uint32_t dst = a_dst + r * 128 + ((chunk ^ (r & 7)) << 4);
-          ptx::cp_async_16(dst, off >= 0 ? args.x + off + k0 : args.x, off >= 0 ? 16u : 0u);
-        }
-        ptx::cp_async_commit();
-        ptx::cp_async_wait<0>();
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(full_bar(slot));
-      }
-      ptx::cp_async_wait<0>();
-      // never leave with bulk copies still writing this CTA's shared memory
-      if (lane == 0 && fills > 0) ptx::mbar_wait_drain(full_bar(slot), (fills - 1) & 1);
-    } else if (tid == kEpiThreads) {
+  if (warp == kEpiThreads / 32) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int fills[kStages] = {0, 0, 0, 0};
+      int issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         const int mt = t / args.n_tiles;
@@ -204,15 +133,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ptx::tma_load_2d(b_dst, &map_b, full_bar(stage), kb * kBK, b_row0);
           ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(stage), kb * kBK, b_row0 + kBM);
           ptx::tma_load_2d(a_dst, &map_a, full_bar(stage), kb * kBK, mt * kBM);
-          ++fills[stage];
+          ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
 #pragma unroll
-      for (int st = 0; st < kStages; ++st)
-        if (fills[st] > 0) ptx::mbar_wait_drain(full_bar(st), (fills[st] - 1) & 1);
+      for (int st = 0; st < kStages; ++st) {
+        const int fills = issued / kStages + (st < issued % kStages ? 1 : 0);
+        if (fills > 0) ptx::mbar_wait_drain(full_bar(st), (fills - 1) & 1);
+      }
     }
-  } else if (warp == 8) {
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (ptx::elect_one()) {
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, kBN);
@@ -247,10 +179,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     // Each warp drains its 32 accumulator rows 32 columns at a time through a
-    // shared staging tile, so that the global stores (gate_up) and the fp32
-    // atomics (down) of one instruction cover whole row segments of 4-8 rows
-    // instead of 32 scattered 16-byte pieces.
-    float* stg = reinterpret_cast<float*>(ctl + 256 + 4 * kBM * 4) + warp * 32 * kStagePitch;
+    // shared staging tile, so that the fp32 atomics of one instruction cover
+    // whole 128-byte row segments of 4 rows instead of 32 scattered 16-byte
+    // pieces.
+    float* stg = reinterpret_cast<float*>(ctl + 256) + warp * 32 * kStagePitch;
     const int r = warp * 32 + lane;  // accumulator row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     int it = 0;
@@ -264,36 +196,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ptx::mbar_wait(tfull_bar(b), tphase, abort_flag)) break;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + lane_off + b * kBN;
-      if (MODE == kGateUp) {
-        // h[pos, n0 + c*32 .. +32] = silu(gate) * up; 8 lanes write one row's 64 bytes
-        const int n0 = nt * kBM;
-        const int row0 = mt * kBM + warp * 32;
-#pragma unroll 1
-        for (int c = 0; c < kBM / 32; ++c) {
-          uint32_t g[32], u[32];
-          ptx::tmem_ld32(tbase + c * 32, g);
-          ptx::tmem_ld32(tbase + kBM + c * 32, u);
-          ptx::tmem_ld_wait();
-          uint32_t* srow = reinterpret_cast<uint32_t*>(stg + lane * kStagePitch);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-            const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
-            const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
-            srow[j] = *reinterpret_cast<const uint32_t*>(&hv);
-          }
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rl = i * 4 + (lane >> 3);
-            const int q = lane & 7;  // 8 bytes of the row's 64
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(stg + rl * kStagePitch) + 2 * q;
-            uint2* dst = reinterpret_cast<uint2*>(args.h + static_cast<size_t>(row0 + rl) * args.I + n0 + c * 32) + q;
-            *dst = make_uint2(src[0], src[1]);
-          }
-          __syncwarp();
-        }
-      } else {
+      {
         const bool valid = sid < args.num_pairs;
         const float w = valid ? __ldg(args.topk_w + sid) : 0.f;
         const int tok = valid ? sid / args.topk : -1;
@@ -330,7 +233,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (warp == 8) ptx::tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem_base, kTmemCols);
   if (tid == 0 && *abort_flag) report_error(args.err, MOE_DEVERR_TIMEOUT);
 }
 
@@ -397,21 +300,6 @@ bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
   return r == CUDA_SUCCESS;
 }
 
-moe_status_t launch_gemm_gate_up(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_ids,
-                                 const int32_t* expert_ids, const int32_t* ntpp, __nv_bfloat16* h, int* err,
-                                 int num_pairs, int topk, int H, int I, int E, cudaStream_t s) {
-  CUtensorMap map_b;
-  if (!make_tmap_bf16_2d(&map_b, w1, static_cast<uint64_t>(E) * 2 * I, H)) return MOE_ERR_CUDA;
-  GemmArgs a{};
-  a.x = x; a.sorted_ids = sorted_ids; a.expert_ids = expert_ids; a.ntpp = ntpp; a.h = h; a.err = err;
-  a.num_pairs = num_pairs; a.topk = topk; a.K = H; a.I = I; a.H = H;
-  a.n_tiles = I / kBM; a.b_rows_per_expert = 2 * I;
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_gemm_kernel<kGateUp>), static_cast<int>(kGemmSmem)))
-    return MOE_ERR_CUDA;
-  moe_gemm_kernel<kGateUp><<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_b, map_b, a);
-  return launch_status();
-}
-
 moe_status_t launch_gemm_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, const int32_t* sorted_ids,
                               const int32_t* expert_ids, const int32_t* ntpp, const float* topk_w, float* y_acc,
                               int* err, int num_pairs, int topk, int cap, int H, int I, int E, cudaStream_t s) {
@@ -420,11 +308,11 @@ moe_status_t launch_gemm_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, c
   if (!make_tmap_bf16_2d(&map_b, w2, static_cast<uint64_t>(E) * H, I)) return MOE_ERR_CUDA;
   GemmArgs a{};
   a.sorted_ids = sorted_ids; a.expert_ids = expert_ids; a.ntpp = ntpp; a.topk_w = topk_w; a.y_acc = y_acc;
-  a.err = err; a.num_pairs = num_pairs; a.topk = topk; a.K = I; a.I = I; a.H = H;
+  a.err = err; a.num_pairs = num_pairs; a.topk = topk; a.K = I; a.H = H;
   a.n_tiles = H / kBN; a.b_rows_per_expert = H;
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_gemm_kernel<kDown>), static_cast<int>(kGemmSmem)))
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_down_kernel), static_cast<int>(kGemmSmem)))
     return MOE_ERR_CUDA;
-  moe_gemm_kernel<kDown><<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_a, map_b, a);
+  moe_down_kernel<<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_a, map_b, a);
   return launch_status();
 }
 
