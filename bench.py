@@ -383,7 +383,7 @@ def bench_lowp(moe, synth, torch, dev, flush, peaks, args):
         qw = qw.view(cfg.E, cfg.N, cfg.K)
         sw = sw.view(cfg.E, cfg.N)
         y = torch.empty((cfg.M, cfg.N), dtype=torch.bfloat16, device=dev)
-        ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+        ws = torch.zeros(moe.gmm_lowp_workspace_size(cfg.M, cfg.K, cfg.N, cfg.E), dtype=torch.uint8, device=dev)
         run = lambda: moe.gmm_lowp(qx, qw, sx, sw, d["expert_offsets"], d["expert_sizes"], torch.bfloat16, y, ws)
         for _ in range(3):
             run()

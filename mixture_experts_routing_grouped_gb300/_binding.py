@@ -145,6 +145,10 @@ def moe_fused_forward_workspace_size(T: int, H: int, I: int, E: int, topk: int) 
     return int(lib().moe_fused_forward_workspace_size(T, H, I, E, topk))
 
 
+def gmm_lowp_workspace_size(M: int, K: int, N: int, E: int) -> int:
+    return int(lib().gmm_lowp_workspace_size(M, K, N, E))
+
+
 def moe_fused_forward(x: torch.Tensor, gating: torch.Tensor, w_gate_up: torch.Tensor, w_down: torch.Tensor,
                       topk: int, renormalize: bool = True, num_expert_group: int = 1, topk_group: int = 1,
                       scoring_func: str = "softmax", routed_scaling_factor: float = 1.0,

@@ -10,17 +10,23 @@
 //   out[m, n] = scales_x[m] * scales_w[e, n] * sum_k q_x[m, k] * q_w[e, n, k]
 //
 // FP8-e4m3 runs natively on tcgen05 (kind::f8f6f4, fp32 accumulation in TMEM).
-// tcgen05 has no integer MMA on sm_103a, so INT8 tiles are brought in by TMA
-// unconverted and widened in shared memory to fp16 (exact for |q| <= 128) by
-// four converter warps; the MMA is then kind::f16 with fp32 accumulation.
+// tcgen05 has no integer MMA on sm_103a, so INT8 codes are widened to fp16
+// (exact for |q| <= 128) and the MMA is kind::f16 with fp32 accumulation: the
+// activation codes once, by a pre-pass into the workspace (every row block is
+// reused by all N / 128 column blocks, so widening it per tile repeated the work
+// N / 128 times and bounded the kernel), the weight codes per tile in shared
+// memory by eight converter warps, after TMA brought them in unconverted. The
+// weight codes (the HBM stream) and the widened activations (L2-resident) move
+// through separate rings, so the codes can be fetched six K steps ahead.
 //
 // Kernel shape (one persistent CTA per SM): warps 0-3 epilogue, warp 4 task
-// claimer + TMA producer, warp 5 TMA-owner of TMEM + MMA issuer, warps 6-9
-// INT8 converters. Tile 128 rows x 128 columns x 128 K; a task is (expert,
-// 128-row block, 128-column block), ordered expert, column block, row block so
-// that CTAs running together share each weight tile in L2. Rows of a block past
-// the expert's end are computed on whatever TMA brought (the next expert's rows
-// or zero fill) and never stored.
+// claimer + TMA producer (FP8: both operands; INT8: weight codes), warp 5
+// owner of TMEM + MMA issuer, INT8 only: warps 6-13 weight converters, warp 14
+// TMA producer of the widened activations. Tile 128 rows x 128 columns x 128 K; a task is
+// (expert, 128-row block, 128-column block), ordered expert, column block, row
+// block so that CTAs running together share each weight tile in L2. Rows of a
+// block past the expert's end are computed on whatever TMA brought (the next
+// expert's rows or zero fill) and never stored.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -30,18 +36,30 @@
 namespace moe {
 
 bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, bool swizzle128);
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
 
 namespace {
 
 constexpr int kLBM = 128, kLBN = 128, kLBK = 128;      // K in elements (= bytes for 8-bit codes)
 constexpr int kTile8 = kLBM * kLBK;                     // 16 KB: one 8-bit operand tile
 constexpr int kF8Stages = 6;                            // fp8: 6 x (A 16 KB + B 16 KB)
-constexpr int kI8Stages = 2;                            // int8: 2 x 32 KB staging + 2 x 64 KB fp16 operands
 constexpr int kTile16 = kLBM * kLBK * 2;                // 32 KB: one fp16 operand tile (2 column blocks)
+constexpr int kI8BStages = 6;                           // int8: 6 x 16 KB weight codes
+constexpr int kI8AStages = 2;                           // int8: 2 x 32 KB widened activations
+constexpr int kI8Ops = 2;                               // int8: 2 x 32 KB widened weight tiles
+constexpr int kI8ConvWarps = 8;
+constexpr int kI8AWarp = 6 + kI8ConvWarps;              // warp 14: activation producer
+constexpr int kI8AOff = kI8BStages * kTile8;            // 96 KB
+constexpr int kI8OpOff = kI8AOff + kI8AStages * kTile16;  // 160 KB
 constexpr int kQ = 4;                                   // task queue slots
-constexpr int kLThreads = 320;
 constexpr int kLTmemCols = 2 * kLBN;
-constexpr size_t kLSmem = 1024 + 192 * 1024 + 512;
+constexpr int kF8Ring = kF8Stages * 2 * kTile8;         // 192 KB
+constexpr int kI8Ring = kI8OpOff + kI8Ops * kTile16;    // 224 KB
+constexpr size_t kLSmem = 1024 + kI8Ring + 512;
+static_assert(kLSmem <= 232448, "shared memory per CTA");
+static_assert(kI8AStages == kI8Ops, "the MMA advances the activation and operand rings together");
+template <bool I8>
+constexpr int lowp_threads() { return 32 * (I8 ? kI8AWarp + 1 : 6); }
 
 struct LowpArgs {
   const float* sx;
@@ -143,8 +161,24 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   hi = *reinterpret_cast<const uint32_t*>(&hb);
 }
 
+// INT8 activation codes -> fp16 (exact), 16 codes per thread and step.
+__global__ void __launch_bounds__(256) widen_i8_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                       size_t n16) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldg(src + i);
+    uint32_t h[8];
+    i8x4_to_f16x4(v.x, h[0], h[1]);
+    i8x4_to_f16x4(v.y, h[2], h[3]);
+    i8x4_to_f16x4(v.z, h[4], h[5]);
+    i8x4_to_f16x4(v.w, h[6], h[7]);
+    dst[2 * i] = make_uint4(h[0], h[1], h[2], h[3]);
+    dst[2 * i + 1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
 template <bool I8>
-__global__ void __launch_bounds__(kLThreads, 1)
+__global__ void __launch_bounds__(lowp_threads<I8>(), 1)
     gmm_lowp_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                     const LowpArgs args) {
   extern __shared__ uint8_t smem_raw[];
@@ -152,12 +186,13 @@ __global__ void __launch_bounds__(kLThreads, 1)
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = raw_addr + pad;
-  constexpr int kStages = I8 ? kI8Stages : kF8Stages;
+  constexpr int kStages = I8 ? kI8BStages : kF8Stages;
   // fp8: stage s = [A 16 KB | B 16 KB] at s*32 KB.
-  // int8: staging s = [A 16 KB | B 16 KB] at s*32 KB (no swizzle); fp16 operands
-  //       o = [A 32 KB | B 32 KB] at 64 KB + o*64 KB, each tile = 2 column blocks of
-  //       [128 rows][128 B] with the 128B swizzle.
-  uint8_t* ctl = smem + 192 * 1024;
+  // int8: weight-code stage s (16 KB, unswizzled) at s*16 KB; widened activations
+  //       a (32 KB: 2 column blocks of [128 rows][128 B], 128B swizzle) at
+  //       96 KB + a*32 KB; widened weight operand o (32 KB, same layout) at
+  //       160 KB + o*32 KB.
+  uint8_t* ctl = smem + (I8 ? kI8Ring : kF8Ring);
   const uint32_t bar0 = ptx::smem_u32(ctl);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };                 // staging / stage landed
   auto empty_bar = [&](int s) { return bar0 + 8u * (8 + s); };          // staging / stage free
@@ -168,23 +203,30 @@ __global__ void __launch_bounds__(kLThreads, 1)
   auto qfull_bar = [&](int q) { return bar0 + 8u * (28 + q); };
   auto qempty_bar = [&](int q) { return bar0 + 8u * (32 + q); };
   const uint32_t done_bar = bar0 + 8u * 36;
-  volatile int* tq = reinterpret_cast<volatile int*>(ctl + 304);       // [kQ] claimed task ids
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 320);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 324);
+  auto afull_bar = [&](int s) { return bar0 + 8u * (37 + s); };         // int8: activations landed
+  auto aempty_bar = [&](int s) { return bar0 + 8u * (39 + s); };        // int8: activations free
+  volatile int* tq = reinterpret_cast<volatile int*>(ctl + 384);       // [kQ] claimed task ids
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 400);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 404);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = args.N / kLBN;
   const int kblocks = args.K / kLBK;
   const int num_tasks = __ldg(args.num_tasks);
-  constexpr int kConsumers = 1 + 128 + (I8 ? 128 : 0);
+  constexpr int kConvThreads = I8 ? 32 * kI8ConvWarps : 0;
+  constexpr int kConsumers = 1 + 128 + kConvThreads + (I8 ? 1 : 0);
 
   if (tid == 0) {
     for (int s = 0; s < 8; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), I8 ? 128 : 1);
+      ptx::mbar_init(empty_bar(s), I8 ? kConvThreads : 1);  // int8: released by the converters
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(afull_bar(s), 1);
+      ptx::mbar_init(aempty_bar(s), 1);
     }
     for (int s = 0; s < 4; ++s) {
-      ptx::mbar_init(ofull_bar(s), 128);
+      ptx::mbar_init(ofull_bar(s), kConvThreads > 0 ? kConvThreads : 1);
       ptx::mbar_init(oempty_bar(s), 1);
       ptx::mbar_init(qfull_bar(s), 1);
       ptx::mbar_init(qempty_bar(s), kConsumers);
@@ -220,7 +262,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int fills[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      int issued = 0;
       for (int it = 0;; ++it) {
         const int q = it % kQ;
         if (!ptx::mbar_wait(qempty_bar(q), (static_cast<uint32_t>(it / kQ) & 1u) ^ 1u, abort_flag)) break;
@@ -233,23 +275,59 @@ __global__ void __launch_bounds__(kLThreads, 1)
         bool ok = true;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
-          const uint32_t dst = sbase + stage * 2 * kTile8;
-          ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * kTile8);
-          ptx::tma_load_2d(dst, &map_x, full_bar(stage), kb * kLBK, k.row0);
-          ptx::tma_load_2d(dst + kTile8, &map_w, full_bar(stage), kb * kLBK, wrow);
-          ++fills[stage];
+          if constexpr (I8) {
+            const uint32_t dst = sbase + stage * kTile8;  // weight codes
+            ptx::mbar_arrive_expect_tx(full_bar(stage), kTile8);
+            ptx::tma_load_2d(dst, &map_w, full_bar(stage), kb * kLBK, wrow);
+          } else {
+            const uint32_t dst = sbase + stage * 2 * kTile8;
+            ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * kTile8);
+            ptx::tma_load_2d(dst, &map_x, full_bar(stage), kb * kLBK, k.row0);
+            ptx::tma_load_2d(dst + kTile8, &map_w, full_bar(stage), kb * kLBK, wrow);
+          }
+          ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
       }
-      for (int s = 0; s < kStages; ++s)
-        if (fills[s] > 0) ptx::mbar_wait_drain(full_bar(s), (fills[s] - 1) & 1);
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) {
+        const int fills = issued / kStages + (s < issued % kStages ? 1 : 0);
+        if (fills > 0) ptx::mbar_wait_drain(full_bar(s), (fills - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (I8 && warp == kI8AWarp) {
+    // ------------------------------------------------------------ int8: widened-activation producer
+    if (lane == 0) {
+      int astage = 0, issued = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int t = next_task(it);
+        if (t < 0 || t >= num_tasks) break;
+        const Task k = decode_task(args, n_tiles, t);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!ptx::mbar_wait(aempty_bar(astage), aphase ^ 1u, abort_flag)) { ok = false; break; }
+          const uint32_t dst = sbase + kI8AOff + astage * kTile16;
+          ptx::mbar_arrive_expect_tx(afull_bar(astage), kTile16);
+          ptx::tma_load_2d(dst, &map_x, afull_bar(astage), kb * kLBK, k.row0);
+          ptx::tma_load_2d(dst + kTile8, &map_x, afull_bar(astage), kb * kLBK + kLBK / 2, k.row0);
+          ++issued;
+          if (++astage == kI8AStages) { astage = 0; aphase ^= 1u; }
+        }
+      }
+#pragma unroll
+      for (int st = 0; st < kI8AStages; ++st) {
+        const int fills = issued / kI8AStages + (st < issued % kI8AStages ? 1 : 0);
+        if (fills > 0) ptx::mbar_wait_drain(afull_bar(st), (fills - 1) & 1);
+      }
     }
     __syncwarp();
   } else if (warp >= 6) {
-    // ------------------------------------------------------------ int8 -> fp16 converters
+    // ------------------------------------------------------------ int8 -> fp16 weight converters
     if constexpr (I8) {
-      const int c = tid - 192;  // 0..127
+      const int c = tid - 192;  // 0..255
       int stage = 0, ostage = 0;
       uint32_t phase = 0, ophase = 0;
       bool ok = true;
@@ -259,15 +337,14 @@ __global__ void __launch_bounds__(kLThreads, 1)
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
           if (!ptx::mbar_wait(oempty_bar(ostage), ophase ^ 1u, abort_flag)) { ok = false; break; }
-          const uint8_t* src = smem + stage * 2 * kTile8;
-          const uint32_t dst = sbase + 64 * 1024 + ostage * 2 * kTile16;
-          // 2 tiles x 128 rows x 8 chunks of 16 bytes; thread c handles chunk (c & 7) of 8 rows per tile
-#pragma unroll 4
-          for (int i = 0; i < 16; ++i) {
-            const int tile = i >> 3;
-            const int r = (c >> 3) + 16 * (i & 7);
-            const int ch = c & 7;  // 16 int8 = k in [ch*16, ch*16+16)
-            const uint4 v = *reinterpret_cast<const uint4*>(src + tile * kTile8 + r * 128 + ch * 16);
+          const uint8_t* src = smem + stage * kTile8;
+          const uint32_t dst = sbase + kI8OpOff + ostage * kTile16;
+          // 128 rows x 8 chunks of 16 codes; thread c takes chunk (c & 7) of rows c/8 + 32i
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = (c >> 3) + 32 * i;
+            const int ch = c & 7;  // codes k in [ch*16, ch*16+16)
+            const uint4 v = *reinterpret_cast<const uint4*>(src + r * 128 + ch * 16);
             uint32_t h[8];
             i8x4_to_f16x4(v.x, h[0], h[1]);
             i8x4_to_f16x4(v.y, h[2], h[3]);
@@ -276,7 +353,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
             // fp16 k index ch*16 .. +16 -> column block cb = ch / 4, 16-byte chunks j0, j0+1 in the 128-byte row
             const int cb = ch >> 2;
             const int j0 = (ch & 3) * 2;
-            const uint32_t rowbase = dst + tile * kTile16 + cb * kTile8 + r * 128;
+            const uint32_t rowbase = dst + cb * kTile8 + r * 128;
             const uint32_t d0 = rowbase + (((j0) ^ (r & 7)) << 4);
             const uint32_t d1 = rowbase + (((j0 + 1) ^ (r & 7)) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d0), "r"(h[0]), "r"(h[1]), "r"(h[2]),
@@ -288,7 +365,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
           ptx::mbar_arrive(ofull_bar(ostage));
           ptx::mbar_arrive(empty_bar(stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
-          if (++ostage == 2) { ostage = 0; ophase ^= 1u; }
+          if (++ostage == kI8Ops) { ostage = 0; ophase ^= 1u; }
         }
       }
     }
@@ -297,8 +374,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
     if (ptx::elect_one()) {
       const uint32_t idesc = I8 ? (ptx::idesc_bf16_f32(kLBM, kLBN) & ~((7u << 7) | (7u << 10)))  // fp16 A/B
                                 : ptx::idesc_e4m3_f32(kLBM, kLBN);
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, ostage = 0;
+      uint32_t phase = 0, ophase = 0;
       bool ok = true;
       for (int it = 0; ok; ++it) {
         const int t = next_task(it);
@@ -309,17 +386,23 @@ __global__ void __launch_bounds__(kLThreads, 1)
         const uint32_t d_tmem = tmem_base + b * kLBN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if constexpr (I8) {
-            if (!ptx::mbar_wait(ofull_bar(stage), phase, abort_flag)) { ok = false; break; }
+            // the activation and widened-weight rings advance together (both 2 deep)
+            if (!ptx::mbar_wait(afull_bar(ostage), ophase, abort_flag) ||
+                !ptx::mbar_wait(ofull_bar(ostage), ophase, abort_flag)) {
+              ok = false;
+              break;
+            }
             ptx::tc_fence_after();
-            const uint32_t a = sbase + 64 * 1024 + stage * 2 * kTile16;
+            const uint32_t a = sbase + kI8AOff + ostage * kTile16;
+            const uint32_t bop = sbase + kI8OpOff + ostage * kTile16;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t off = (kk >> 2) * kTile8 + (kk & 3) * 32;
-              ptx::mma_f16(d_tmem, ptx::sdesc_sw128(a + off), ptx::sdesc_sw128(a + kTile16 + off), idesc,
-                           (kb | kk) != 0);
+              ptx::mma_f16(d_tmem, ptx::sdesc_sw128(a + off), ptx::sdesc_sw128(bop + off), idesc, (kb | kk) != 0);
             }
-            ptx::mma_commit(oempty_bar(stage));
-            if (++stage == 2) { stage = 0; phase ^= 1u; }
+            ptx::mma_commit(oempty_bar(ostage));
+            ptx::mma_commit(aempty_bar(ostage));
+            if (++ostage == kI8Ops) { ostage = 0; ophase ^= 1u; }
           } else {
             if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
             ptx::tc_fence_after();
@@ -395,14 +478,18 @@ __global__ void __launch_bounds__(kLThreads, 1)
 
 }  // namespace
 
-size_t lowp_workspace_bytes(int E) { return kWsHeader + align_up(static_cast<size_t>(E + 1) * 4, 256); }
+// Header, per-expert row-block prefix, then (INT8 inputs) the fp16 copy of the activation codes.
+size_t lowp_meta_bytes(int E) { return kWsHeader + align_up(static_cast<size_t>(E + 1) * 4, 256); }
+size_t lowp_workspace_bytes(int M, int K, int E) {
+  return lowp_meta_bytes(E) + align_up(static_cast<size_t>(M) * K * 2, 256);
+}
 
 }  // namespace moe
 
 extern "C" size_t gmm_lowp_workspace_size(int M, int K, int N, int E) {
-  (void)M; (void)K; (void)N;
-  if (E <= 0) return 0;
-  return moe::lowp_workspace_bytes(E);
+  (void)N;
+  if (E <= 0 || M < 0 || K < 0) return 0;
+  return moe::lowp_workspace_bytes(M, K, E);
 }
 
 extern "C" moe_status_t gmm_lowp(const void* input, const void* weights, const float* scales_x,
@@ -418,8 +505,9 @@ extern "C" moe_status_t gmm_lowp(const void* input, const void* weights, const f
   if (K % kLBK != 0 || N % kLBN != 0) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(input) || !aligned16(weights) || !aligned16(scales_w) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(E) * N >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
-  if (!ws || ws_bytes < lowp_workspace_bytes(E) || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
-    return MOE_ERR_WORKSPACE;
+  const bool i8 = in_dt == MOE_DT_I8;
+  const size_t need = i8 ? lowp_workspace_bytes(M, K, E) : lowp_meta_bytes(E);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
   if (M == 0) return MOE_OK;
   cudaStream_t s = as_stream(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -432,9 +520,19 @@ extern "C" moe_status_t gmm_lowp(const void* input, const void* weights, const f
                                       err);
   moe_status_t st = launch_status();
   if (st != MOE_OK) return st;
-  const bool i8 = in_dt == MOE_DT_I8;
   CUtensorMap map_x, map_w;
-  if (!make_tmap_u8_2d(&map_x, input, M, K, !i8)) return MOE_ERR_CUDA;
+  if (i8) {
+    // widen the activation codes once; the kernel loads them as fp16 tiles (a
+    // 2-byte tensor map: TMA moves bytes, the bf16 element type only sizes them)
+    void* xh = w + lowp_meta_bytes(E);
+    const size_t n16 = static_cast<size_t>(M) * K / 16;
+    const int grid = static_cast<int>(std::min<size_t>((n16 + 255) / 256, static_cast<size_t>(num_sms()) * 8));
+    widen_i8_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(input), static_cast<uint4*>(xh), n16);
+    if ((st = launch_status()) != MOE_OK) return st;
+    if (!make_tmap_bf16_2d(&map_x, xh, M, K)) return MOE_ERR_CUDA;
+  } else if (!make_tmap_u8_2d(&map_x, input, M, K, true)) {
+    return MOE_ERR_CUDA;
+  }
   if (!make_tmap_u8_2d(&map_w, weights, static_cast<uint64_t>(E) * N, K, !i8)) return MOE_ERR_CUDA;
   LowpArgs a{};
   a.sx = scales_x; a.sw = scales_w; a.offsets = expert_offsets; a.sizes = expert_sizes; a.mt_prefix = mt_prefix;
@@ -444,8 +542,8 @@ extern "C" moe_status_t gmm_lowp(const void* input, const void* weights, const f
                       : reinterpret_cast<const void*>(gmm_lowp_kernel<false>);
   if (!ensure_smem_attr(fn, static_cast<int>(kLSmem))) return MOE_ERR_CUDA;
   if (i8)
-    gmm_lowp_kernel<true><<<num_sms(), kLThreads, kLSmem, s>>>(map_x, map_w, a);
+    gmm_lowp_kernel<true><<<num_sms(), lowp_threads<true>(), kLSmem, s>>>(map_x, map_w, a);
   else
-    gmm_lowp_kernel<false><<<num_sms(), kLThreads, kLSmem, s>>>(map_x, map_w, a);
+    gmm_lowp_kernel<false><<<num_sms(), lowp_threads<false>(), kLSmem, s>>>(map_x, map_w, a);
   return launch_status();
 }

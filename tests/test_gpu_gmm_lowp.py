@@ -30,7 +30,9 @@ def _to_dev(codes, dt):
 def _run(qx, qw, sx, sw, sizes, dt, out_dtype):
     import mixture_experts_routing_grouped_gb300 as moe
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
-    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    M, K = qx.shape
+    E, N, _ = qw.shape
+    ws = torch.zeros(moe.gmm_lowp_workspace_size(M, K, N, E), dtype=torch.uint8, device="cuda")
     out = moe.gmm_lowp(_to_dev(qx, dt), _to_dev(qw, dt), torch.from_numpy(sx.astype(np.float32)).cuda(),
                        torch.from_numpy(sw.astype(np.float32)).cuda(), torch.from_numpy(off).cuda(),
                        torch.from_numpy(np.asarray(sizes, dtype=np.int32)).cuda(), out_dtype=out_dtype, ws=ws)
@@ -95,7 +97,7 @@ def test_gmm_inconsistent_metadata_is_reported_and_skipped():
     off = torch.tensor([0, 32, 64], dtype=torch.int32, device="cuda")
     sizes = torch.tensor([32, 40], dtype=torch.int32, device="cuda")   # expert 1 does not add up
     out = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
-    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(moe.gmm_lowp_workspace_size(M, K, N, E), dtype=torch.uint8, device="cuda")
     moe.gmm_lowp(qx, qw, torch.ones(M, device="cuda"), torch.ones(E, N, device="cuda"), off, sizes,
                  out_dtype=torch.float32, out=out, ws=ws)
     code = moe.moe_check_device_error(ws)

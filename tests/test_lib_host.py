@@ -91,3 +91,10 @@ def test_fused_validation_and_sizes(L):
     need = L.moe_fused_forward_workspace_size(64, 512, 256, 8, 2)
     assert f(*args(512, 256, need - 1)) == 3
     assert f(*args(512, 256, need, ctypes.c_void_p(0x10010))) == 3  # workspace not 256-byte aligned
+
+
+def test_gmm_lowp_workspace_holds_the_widened_activations(L):
+    # INT8 inputs are widened to fp16 once, into the workspace: M*K*2 bytes beyond the metadata
+    for M, K, N, E in ((2048, 4096, 4096, 32), (1, 128, 128, 1), (0, 256, 128, 4)):
+        assert L.gmm_lowp_workspace_size(M, K, N, E) >= M * K * 2 + 256
+    assert L.gmm_lowp_workspace_size(16, 128, 128, 0) == 0
