@@ -16,8 +16,8 @@
 // reused by all N / 128 column blocks, so widening it per tile repeated the work
 // N / 128 times and bounded the kernel), the weight codes per tile in shared
 // memory by eight converter warps, after TMA brought them in unconverted. The
-// weight codes (the HBM stream) and the widened activations (L2-resident) move
-// through separate rings, so the codes can be fetched six K steps ahead.
+// weight codes (the HBM stream), the widened activations (L2-resident) and the
+// widened weights move through separate rings.
 //
 // Kernel shape (one persistent CTA per SM): warps 0-3 epilogue, warp 4 task
 // claimer + TMA producer (FP8: both operands; INT8: weight codes), warp 5
@@ -44,20 +44,19 @@ constexpr int kLBM = 128, kLBN = 128, kLBK = 128;      // K in elements (= bytes
 constexpr int kTile8 = kLBM * kLBK;                     // 16 KB: one 8-bit operand tile
 constexpr int kF8Stages = 6;                            // fp8: 6 x (A 16 KB + B 16 KB)
 constexpr int kTile16 = kLBM * kLBK * 2;                // 32 KB: one fp16 operand tile (2 column blocks)
-constexpr int kI8BStages = 6;                           // int8: 6 x 16 KB weight codes
-constexpr int kI8AStages = 2;                           // int8: 2 x 32 KB widened activations
+constexpr int kI8BStages = 4;                           // int8: 4 x 16 KB weight codes
+constexpr int kI8AStages = 3;                           // int8: 3 x 32 KB widened activations
 constexpr int kI8Ops = 2;                               // int8: 2 x 32 KB widened weight tiles
 constexpr int kI8ConvWarps = 8;
 constexpr int kI8AWarp = 6 + kI8ConvWarps;              // warp 14: activation producer
-constexpr int kI8AOff = kI8BStages * kTile8;            // 96 KB
-constexpr int kI8OpOff = kI8AOff + kI8AStages * kTile16;  // 160 KB
+constexpr int kI8AOff = kI8BStages * kTile8;
+constexpr int kI8OpOff = kI8AOff + kI8AStages * kTile16;
 constexpr int kQ = 4;                                   // task queue slots
 constexpr int kLTmemCols = 2 * kLBN;
 constexpr int kF8Ring = kF8Stages * 2 * kTile8;         // 192 KB
 constexpr int kI8Ring = kI8OpOff + kI8Ops * kTile16;    // 224 KB
 constexpr size_t kLSmem = 1024 + kI8Ring + 512;
 static_assert(kLSmem <= 232448, "shared memory per CTA");
-static_assert(kI8AStages == kI8Ops, "the MMA advances the activation and operand rings together");
 template <bool I8>
 constexpr int lowp_threads() { return 32 * (I8 ? kI8AWarp + 1 : 6); }
 
@@ -189,9 +188,8 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
   constexpr int kStages = I8 ? kI8BStages : kF8Stages;
   // fp8: stage s = [A 16 KB | B 16 KB] at s*32 KB.
   // int8: weight-code stage s (16 KB, unswizzled) at s*16 KB; widened activations
-  //       a (32 KB: 2 column blocks of [128 rows][128 B], 128B swizzle) at
-  //       96 KB + a*32 KB; widened weight operand o (32 KB, same layout) at
-  //       160 KB + o*32 KB.
+  //       a (32 KB: 2 column blocks of [128 rows][128 B], 128B swizzle) after the
+  //       code ring; widened weight operand o (32 KB, same layout) after those.
   uint8_t* ctl = smem + (I8 ? kI8Ring : kF8Ring);
   const uint32_t bar0 = ptx::smem_u32(ctl);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };                 // staging / stage landed
@@ -204,7 +202,7 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
   auto qempty_bar = [&](int q) { return bar0 + 8u * (32 + q); };
   const uint32_t done_bar = bar0 + 8u * 36;
   auto afull_bar = [&](int s) { return bar0 + 8u * (37 + s); };         // int8: activations landed
-  auto aempty_bar = [&](int s) { return bar0 + 8u * (39 + s); };        // int8: activations free
+  auto aempty_bar = [&](int s) { return bar0 + 8u * (41 + s); };        // int8: activations free
   volatile int* tq = reinterpret_cast<volatile int*>(ctl + 384);       // [kQ] claimed task ids
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 400);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 404);
@@ -221,7 +219,7 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), I8 ? kConvThreads : 1);  // int8: released by the converters
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kI8AStages; ++s) {
       ptx::mbar_init(afull_bar(s), 1);
       ptx::mbar_init(aempty_bar(s), 1);
     }
@@ -327,7 +325,7 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
   } else if (warp >= 6) {
     // ------------------------------------------------------------ int8 -> fp16 weight converters
     if constexpr (I8) {
-      const int c = tid - 192;  // 0..255
+      const int c = tid - 192;  // 0 .. kConvThreads-1
       int stage = 0, ostage = 0;
       uint32_t phase = 0, ophase = 0;
       bool ok = true;
@@ -339,10 +337,10 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
           if (!ptx::mbar_wait(oempty_bar(ostage), ophase ^ 1u, abort_flag)) { ok = false; break; }
           const uint8_t* src = smem + stage * kTile8;
           const uint32_t dst = sbase + kI8OpOff + ostage * kTile16;
-          // 128 rows x 8 chunks of 16 codes; thread c takes chunk (c & 7) of rows c/8 + 32i
+          // 128 rows x 8 chunks of 16 codes; thread c takes chunk (c & 7) of rows c/8 + (kConvThreads/8) i
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = (c >> 3) + 32 * i;
+          for (int i = 0; i < 1024 / kConvThreads; ++i) {
+            const int r = (c >> 3) + (kConvThreads / 8) * i;
             const int ch = c & 7;  // codes k in [ch*16, ch*16+16)
             const uint4 v = *reinterpret_cast<const uint4*>(src + r * 128 + ch * 16);
             uint32_t h[8];
@@ -374,8 +372,8 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
     if (ptx::elect_one()) {
       const uint32_t idesc = I8 ? (ptx::idesc_bf16_f32(kLBM, kLBN) & ~((7u << 7) | (7u << 10)))  // fp16 A/B
                                 : ptx::idesc_e4m3_f32(kLBM, kLBN);
-      int stage = 0, ostage = 0;
-      uint32_t phase = 0, ophase = 0;
+      int stage = 0, ostage = 0, astage = 0;
+      uint32_t phase = 0, ophase = 0, aphase = 0;
       bool ok = true;
       for (int it = 0; ok; ++it) {
         const int t = next_task(it);
@@ -386,14 +384,13 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
         const uint32_t d_tmem = tmem_base + b * kLBN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if constexpr (I8) {
-            // the activation and widened-weight rings advance together (both 2 deep)
-            if (!ptx::mbar_wait(afull_bar(ostage), ophase, abort_flag) ||
+            if (!ptx::mbar_wait(afull_bar(astage), aphase, abort_flag) ||
                 !ptx::mbar_wait(ofull_bar(ostage), ophase, abort_flag)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            const uint32_t a = sbase + kI8AOff + ostage * kTile16;
+            const uint32_t a = sbase + kI8AOff + astage * kTile16;
             const uint32_t bop = sbase + kI8OpOff + ostage * kTile16;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -401,8 +398,9 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
               ptx::mma_f16(d_tmem, ptx::sdesc_sw128(a + off), ptx::sdesc_sw128(bop + off), idesc, (kb | kk) != 0);
             }
             ptx::mma_commit(oempty_bar(ostage));
-            ptx::mma_commit(aempty_bar(ostage));
+            ptx::mma_commit(aempty_bar(astage));
             if (++ostage == kI8Ops) { ostage = 0; ophase ^= 1u; }
+            if (++astage == kI8AStages) { astage = 0; aphase ^= 1u; }
           } else {
             if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
             ptx::tc_fence_after();
