@@ -181,11 +181,11 @@ MOE_API moe_status_t moe_fused_forward_noalloc(const void* x, const float* gatin
  * moe_set_stage_events -- optional per-stage timing of moe_fused_forward (not in the
  * pages; instrumentation only). While set, every moe_fused_forward call made by
  * the calling host thread records events[0] on its stream before the routing
- * kernel and events[i] after its i-th step: 1 routing (which also clears the
- * fp32 accumulator), 2 align, 3 (empty: kept for a stable numbering), 4 gate_up
- * GEMM, 5 down GEMM, 6 cast to bf16 (n >= 7 records all). The
- * events are cudaEvent_t handles owned by the caller. events = NULL or n = 0
- * switches the recording off.
+ * kernel and events[i] after its i-th step: 1 routing, 2 align, 3 gate_up GEMM,
+ * 4 down GEMM, 5 cast to bf16 (n >= 6 records all). The fp32 accumulator of the
+ * down pass is cleared inside step 3 (prefill kernels) or step 1 (decode
+ * kernels). The events are cudaEvent_t handles owned by the caller. events =
+ * NULL or n = 0 switches the recording off.
  */
 MOE_API void moe_set_stage_events(void* const* events, int n);
 

@@ -28,7 +28,7 @@ moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m,
                           cudaStream_t s, int32_t* sorted_tok, int topk);
 moe_status_t launch_gemm_gate_up_pairs(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_tok,
                                        const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
-                                       int H, int I, int E, cudaStream_t s);
+                                       int H, int I, int E, float* y_clear, size_t y_clear_floats, cudaStream_t s);
 bool gate_up_pair2_supported(int I);
 moe_status_t launch_gemm_gate_up_pair2(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_tok,
                                        const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
@@ -85,13 +85,24 @@ Plan choose_plan(int T, int E, int topk) {
   return p;
 }
 
-__global__ void cast_f32_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const float4 v = src[i];
-    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
-    dst[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+// y = bf16(y_acc): four independent 16-byte loads in flight per thread (one at a
+// time left the kernel latency-bound on the just-written, L2-resident rows).
+__global__ void __launch_bounds__(256) cast_f32_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
+                                                            size_t n4) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4; i += 4 * stride) {
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (i + j * stride < n4) v[j] = src[i + j * stride];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (i + j * stride >= n4) break;
+      const __nv_bfloat162 a = __floats2bfloat162_rn(v[j].x, v[j].y);
+      const __nv_bfloat162 b = __floats2bfloat162_rn(v[j].z, v[j].w);
+      dst[i + j * stride] =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    }
   }
 }
 
@@ -125,7 +136,7 @@ inline void stage_mark(int i, cudaStream_t s) {
 }
 
 int grid_for(size_t n4) {
-  const size_t want = (n4 + 255) / 256;
+  const size_t want = (n4 + 1023) / 1024;  // 256 threads x 4 elements
   const size_t cap = static_cast<size_t>(num_sms() > 0 ? num_sms() : 148) * 8;
   return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
 }
@@ -178,10 +189,14 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   float* y_acc = reinterpret_cast<float*>(w + L.y_acc);
   const int num_pairs = T * topk;
 
+  // The fp32 accumulator of the down pass is cleared by the one-SM gate_up
+  // kernel's epilogue warps while its first tiles run, else by the routing
+  // kernel (each token's row).
+  const bool gate_up_clears = !plan.swap && !(plan.pair_gate_up && gate_up_pair2_supported(I));
   stage_mark(0, s);
-  // the routing kernel also clears each token's row of the fp32 accumulator
   st = launch_grouped_topk(gating, T, E, num_expert_group, topk_group, topk, scoring, renormalize,
-                           routed_scaling_factor, topk_weights, topk_ids, s, y_acc, H, nullptr, 0);
+                           routed_scaling_factor, topk_weights, topk_ids, s, gate_up_clears ? nullptr : y_acc, H,
+                           nullptr, 0);
   if (st != MOE_OK) return st;
   stage_mark(1, s);
   st = launch_align(topk_ids, num_pairs, E, plan.block_m, sorted_ids, expert_ids, offsets, ntpp, w + L.align_scratch,
@@ -189,7 +204,6 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   if (st != MOE_OK) return st;
   stage_mark(2, s);
   const size_t n4 = static_cast<size_t>(T) * H / 4;
-  stage_mark(3, s);
   if (plan.swap)
     st = launch_swap_gate_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_gate_up),
                              sorted_ids, offsets, h, err, num_pairs, topk, H, I, E, plan.nmax, s);
@@ -200,9 +214,9 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   else
     st = launch_gemm_gate_up_pairs(static_cast<const __nv_bfloat16*>(x),
                                    static_cast<const __nv_bfloat16*>(w_gate_up), sorted_tok, offsets, h, err,
-                                   num_pairs, topk, H, I, E, s);
+                                   num_pairs, topk, H, I, E, y_acc, static_cast<size_t>(T) * H, s);
   if (st != MOE_OK) return st;
-  stage_mark(4, s);
+  stage_mark(3, s);
   if (plan.swap)
     st = launch_swap_down(h, static_cast<const __nv_bfloat16*>(w_down), sorted_ids, offsets, topk_weights, y_acc, err,
                           num_pairs, topk, L.cap, H, I, E, plan.nmax, s);
@@ -213,10 +227,10 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
     st = launch_gemm_down(h, static_cast<const __nv_bfloat16*>(w_down), sorted_ids, expert_ids, ntpp, topk_weights,
                           y_acc, err, num_pairs, topk, L.cap, H, I, E, s);
   if (st != MOE_OK) return st;
-  stage_mark(5, s);
+  stage_mark(4, s);
   cast_f32_bf16_kernel<<<grid_for(n4), 256, 0, s>>>(reinterpret_cast<const float4*>(y_acc),
                                                     reinterpret_cast<uint2*>(y), n4);
   if ((st = launch_status()) != MOE_OK) return st;
-  stage_mark(6, s);
+  stage_mark(5, s);
   return MOE_OK;
 }

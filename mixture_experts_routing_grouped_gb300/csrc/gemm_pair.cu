@@ -65,6 +65,8 @@ struct GemmArgs {
   int I;
   int n_tiles;
   int b_rows_per_expert;
+  float4* clear;    // fp32 accumulator of the down pass to zero (null: none)
+  size_t clear_n4;  // its length in float4
 };
 
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
@@ -282,6 +284,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     float* stg = stg_all + warp * 32 * kStagePitch;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    if (args.clear) {
+      // Zero this CTA's share of the down pass's accumulator while the first
+      // tile's main loop runs (the down kernel starts after this kernel ends).
+      const size_t per = (args.clear_n4 + gridDim.x - 1) / gridDim.x;
+      const size_t lo = per * blockIdx.x;
+      const size_t hi = lo + per < args.clear_n4 ? lo + per : args.clear_n4;
+      for (size_t i = lo + tid; i < hi; i += 32 * kEpiWarps) args.clear[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     int it = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
       const TileInfo ti = decode_tile(pfx, args.offsets, args.E, args.n_tiles, t);
@@ -334,7 +344,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 moe_status_t launch_gemm_gate_up_pairs(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_tok,
                                        const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
-                                       int H, int I, int E, cudaStream_t s) {
+                                       int H, int I, int E, float* y_clear, size_t y_clear_floats, cudaStream_t s) {
   (void)num_pairs; (void)topk;
   using namespace pair;
   CUtensorMap map_b;
@@ -343,6 +353,7 @@ moe_status_t launch_gemm_gate_up_pairs(const __nv_bfloat16* x, const __nv_bfloat
   a.x = x; a.sorted_tok = sorted_tok; a.offsets = offsets; a.h = h; a.err = err;
   a.E = E; a.K = H; a.I = I;
   a.n_tiles = I / kHalf; a.b_rows_per_expert = 2 * I;
+  a.clear = reinterpret_cast<float4*>(y_clear); a.clear_n4 = y_clear ? y_clear_floats / 4 : 0;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_gate_up_kernel), static_cast<int>(kGemmSmem)))
     return MOE_ERR_CUDA;
   moe_gate_up_kernel<<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_b, a);
