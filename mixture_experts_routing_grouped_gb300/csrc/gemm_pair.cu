@@ -17,10 +17,12 @@
 // short next to the main loop). An expert with an odd number of blocks ends
 // with a one-block tile.
 //
-// Kernel shape (one persistent CTA per SM, 384 threads): warps 0-3 epilogue
-// (both row halves, TMEM lane quarter = warp), warp 4 sends the weight tile of
-// every ring slot by TMA, warps 5-10 gather (warps 5+2s and 6+2s own the two row
-// halves of ring slot s), warp 11 owns TMEM and issues the MMAs. A gather lane
+// Kernel shape (one persistent CTA per SM, 512 threads): warps 0-7 epilogue
+// (TMEM lane quarter = warp % 4, column chunks split between warps w and w+4, so
+// that the single accumulator is drained -- and the next tile's MMAs start --
+// in half the time), warp 8 sends the weight tile of every ring slot by TMA,
+// warps 9-14 gather (warps 9+2s and 10+2s own the two row halves of ring slot
+// s), warp 15 owns TMEM and issues the MMAs. A gather lane
 // keeps the source offsets of its 32 rows of the tile in registers, so that its
 // cp.async instructions issue back to back (reading each offset from shared
 // memory between them made the gather issue-bound), and no gather lane waits
@@ -44,13 +46,13 @@ constexpr int kStages = 3;
 constexpr int kHalfBytes = kHalf * kBK * 2;
 constexpr int kABytes = 2 * kHalfBytes;
 constexpr int kBBytes = kBN * kBK * 2;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each draining half of the column chunks
 constexpr int kTmaWarp = kEpiWarps;
 constexpr int kGatherWarp0 = kEpiWarps + 1;
 constexpr int kMmaWarp = kGatherWarp0 + 2 * kStages;
 constexpr int kGemmThreads = 32 * (kMmaWarp + 1);
 constexpr int kTmemCols = 2 * kBN;
-constexpr int kStagePitch = 36;
+constexpr int kStagePitch = 18;  // 32-bit words per staged row: 16 bf16 pairs, 8-byte aligned rows
 constexpr size_t kCtlBytes = 256 + 4 * (MOE_MAX_EXPERTS + 1) + 12 + kEpiWarps * 32 * kStagePitch * 4;
 constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + kCtlBytes;
 
@@ -283,7 +285,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else {
     float* stg = stg_all + warp * 32 * kStagePitch;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int quarter = warp & 3;       // TMEM lane quarter (rows 32*quarter ..)
+    const int cpart = warp >> 2;        // column chunks [2*cpart, 2*cpart + 2) of each row half
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     if (args.clear) {
       // Zero this CTA's share of the down pass's accumulator while the first
       // tile's main loop runs (the down kernel starts after this kernel ends).
@@ -300,9 +304,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int n0 = ti.nt * kHalf;
       for (int half = 0; half < ti.nblk; ++half) {
         const uint32_t tbase = tmem_base + lane_off + half * kBN;
-        const int rowbase = ti.row0 + half * kHalf + warp * 32;
+        const int rowbase = ti.row0 + half * kHalf + quarter * 32;
 #pragma unroll 1
-        for (int c = 0; c < kHalf / 32; ++c) {
+        for (int c = 2 * cpart; c < 2 * cpart + 2; ++c) {
           uint32_t g[32], u[32];
           ptx::tmem_ld32(tbase + c * 32, g);
           ptx::tmem_ld32(tbase + kHalf + c * 32, u);
