@@ -20,7 +20,9 @@
 // Walking every range in order makes the sort stable; no atomics decide
 // positions. Optionally (the fused forward) the token of every sorted position,
 // pair / topk or -1 for padding, is written alongside, so that the grouped GEMMs
-// read gather rows without a division.
+// read gather rows without a division. The first kernel also zeroes one word
+// for the caller (the fused forward's gate_up tile counter), so that the
+// following kernel on the stream starts from zero without a separate launch.
 #include "common.cuh"
 
 #include <algorithm>
@@ -50,7 +52,7 @@ __global__ void __launch_bounds__(kAlignThreads)
                             int nchunks, int32_t* __restrict__ chunk_base, int* __restrict__ done,
                             int32_t* __restrict__ sorted_ids, int32_t* __restrict__ sorted_tok,
                             int32_t* __restrict__ expert_ids, int32_t* __restrict__ expert_offsets,
-                            int32_t* __restrict__ ntpp, int* __restrict__ err) {
+                            int32_t* __restrict__ ntpp, int* __restrict__ err, int* __restrict__ zero_word) {
   __shared__ int hist[MOE_MAX_EXPERTS];
   __shared__ int warp_tot[kAlignWarps];
   __shared__ int is_last;
@@ -59,6 +61,7 @@ __global__ void __launch_bounds__(kAlignThreads)
   __shared__ int seg_padded[MOE_MAX_EXPERTS];
   int* seg_start = hist;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (zero_word && blockIdx.x == 0 && tid == 0) *zero_word = 0;
   for (int e = tid; e < E; e += kAlignThreads) hist[e] = 0;
   __syncthreads();
   const int lo = blockIdx.x * chunk;
@@ -216,9 +219,10 @@ constexpr int kSmallScan = 65536;
 
 __global__ void __launch_bounds__(kAlignThreads)
     align_hist_kernel(const int32_t* __restrict__ ids, int num_pairs, int E, int chunk,
-                      int32_t* __restrict__ hists, int* __restrict__ err) {
+                      int32_t* __restrict__ hists, int* __restrict__ err, int* __restrict__ zero_word) {
   __shared__ int hist[MOE_MAX_EXPERTS];
   const int tid = threadIdx.x;
+  if (zero_word && blockIdx.x == 0 && tid == 0) *zero_word = 0;
   for (int e = tid; e < E; e += kAlignThreads) hist[e] = 0;
   __syncthreads();
   const int lo = blockIdx.x * chunk;
@@ -361,13 +365,13 @@ size_t align_scratch_bytes(int num_pairs, int E) {
 
 moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m, int32_t* sorted_ids,
                           int32_t* expert_ids, int32_t* expert_offsets, int32_t* ntpp, void* scratch, int* err,
-                          cudaStream_t s, int32_t* sorted_tok, int topk) {
+                          cudaStream_t s, int32_t* sorted_tok, int topk, int* zero_word) {
   const int cap = static_cast<int>(align_max_padded(num_pairs, E, block_m));
   const AlignPlan p = align_plan(num_pairs);
   int* done = static_cast<int*>(scratch);
   int32_t* chunk_base = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + 256);
   if (p.nchunks * E <= kSmallScan) {
-    align_hist_kernel<<<p.nchunks, kAlignThreads, 0, s>>>(ids, num_pairs, E, p.chunk, chunk_base, err);
+    align_hist_kernel<<<p.nchunks, kAlignThreads, 0, s>>>(ids, num_pairs, E, p.chunk, chunk_base, err, zero_word);
     moe_status_t st = launch_status();
     if (st != MOE_OK) return st;
     const size_t smem = static_cast<size_t>(kAlignWarps + 3) * E * sizeof(int);
@@ -381,7 +385,7 @@ moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m,
   }
   align_count_scan_kernel<<<p.nchunks, kAlignThreads, 0, s>>>(ids, num_pairs, E, block_m, cap, p.chunk, p.nchunks,
                                                               chunk_base, done, sorted_ids, sorted_tok,
-                                                              expert_ids, expert_offsets, ntpp, err);
+                                                              expert_ids, expert_offsets, ntpp, err, zero_word);
   moe_status_t st = launch_status();
   if (st != MOE_OK) return st;
   const size_t smem = static_cast<size_t>(kAlignWarps) * E * sizeof(int);
@@ -419,5 +423,5 @@ extern "C" moe_status_t moe_align_block_size(const int32_t* topk_ids, int num_pa
   uint8_t* w = static_cast<uint8_t*>(ws);
   return moe::launch_align(topk_ids, num_pairs, E, block_m, sorted_token_ids, expert_ids, expert_offsets,
                            num_tokens_post_padded, w + moe::kWsHeader, reinterpret_cast<int*>(w),
-                           moe::as_stream(stream), nullptr, 0);
+                           moe::as_stream(stream), nullptr, 0, nullptr);
 }

@@ -25,10 +25,11 @@ size_t align_max_padded(int num_pairs, int E, int block_m);
 size_t align_scratch_bytes(int num_pairs, int E);
 moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m, int32_t* sorted_ids,
                           int32_t* expert_ids, int32_t* expert_offsets, int32_t* ntpp, void* scratch, int* err,
-                          cudaStream_t s, int32_t* sorted_tok, int topk);
+                          cudaStream_t s, int32_t* sorted_tok, int topk, int* zero_word);
 moe_status_t launch_gemm_gate_up_pairs(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_tok,
                                        const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
-                                       int H, int I, int E, float* y_clear, size_t y_clear_floats, cudaStream_t s);
+                                       int H, int I, int E, float* y_clear, size_t y_clear_floats,
+                                       int* tile_counter, cudaStream_t s);
 bool gate_up_pair2_supported(int I);
 moe_status_t launch_gemm_gate_up_pair2(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_tok,
                                        const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
@@ -180,6 +181,7 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   cudaStream_t s = as_stream(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   int* err = reinterpret_cast<int*>(w);
+  int* tile_counter = err + 1;  // gate_up tile claims: zeroed by the align step
   int32_t* sorted_ids = reinterpret_cast<int32_t*>(w + L.sorted_ids);
   int32_t* sorted_tok = reinterpret_cast<int32_t*>(w + L.sorted_tok);
   int32_t* expert_ids = reinterpret_cast<int32_t*>(w + L.expert_ids);
@@ -200,7 +202,7 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   if (st != MOE_OK) return st;
   stage_mark(1, s);
   st = launch_align(topk_ids, num_pairs, E, plan.block_m, sorted_ids, expert_ids, offsets, ntpp, w + L.align_scratch,
-                    err, s, sorted_tok, topk);
+                    err, s, sorted_tok, topk, tile_counter);
   if (st != MOE_OK) return st;
   stage_mark(2, s);
   const size_t n4 = static_cast<size_t>(T) * H / 4;
@@ -214,7 +216,7 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   else
     st = launch_gemm_gate_up_pairs(static_cast<const __nv_bfloat16*>(x),
                                    static_cast<const __nv_bfloat16*>(w_gate_up), sorted_tok, offsets, h, err,
-                                   num_pairs, topk, H, I, E, y_acc, static_cast<size_t>(T) * H, s);
+                                   num_pairs, topk, H, I, E, y_acc, static_cast<size_t>(T) * H, tile_counter, s);
   if (st != MOE_OK) return st;
   stage_mark(3, s);
   if (plan.swap)

@@ -17,16 +17,32 @@
 // short next to the main loop). An expert with an odd number of blocks ends
 // with a one-block tile.
 //
+// Tiles are handed out dynamically (the low-precision GMM article's dynamic
+// task scheduling): a CTA starts on tile blockIdx.x and its TMA warp claims
+// each further tile from an atomic counter (zeroed by the align step) a few K
+// steps before the current tile's last weight load, then broadcasts the claimed
+// id to the gather, MMA and epilogue warps through a 4-entry shared-memory
+// queue. Tiles of two row blocks cost twice as much MMA work as an expert's odd
+// last block; a fixed round-robin left the busiest SM about a fifth above the
+// mean, claiming keeps every SM busy until the tiles run out. The claim order
+// stays expert-major, so the CTAs in flight share an expert's weights and rows
+// in L2.
+//
+// A K step is 32 columns (64-byte rows, 64B swizzle), so that the 192 KB ring
+// has six 32 KB slots: a slot's gathered rows and weight tile land 1-3 us after
+// it is freed (L2 and HBM latency under load), and the six slots keep about
+// five K steps of MMA work queued against that, where three 64-column slots
+// left the MMA waiting for data for about 40 % of the kernel.
+//
 // Kernel shape (one persistent CTA per SM, 512 threads): warps 0-7 epilogue
 // (TMEM lane quarter = warp % 4, column chunks split between warps w and w+4, so
 // that the single accumulator is drained -- and the next tile's MMAs start --
 // in half the time), warp 8 sends the weight tile of every ring slot by TMA,
-// warps 9-14 gather (warps 9+2s and 10+2s own the two row halves of ring slot
-// s), warp 15 owns TMEM and issues the MMAs. A gather lane
-// keeps the source offsets of its 32 rows of the tile in registers, so that its
-// cp.async instructions issue back to back (reading each offset from shared
-// memory between them made the gather issue-bound), and no gather lane waits
-// for a TMA issue. The per-expert pair counts are prefix-summed in shared memory
+// warps 9-14 gather (warp 9+s fills both row halves of ring slot s), warp 15
+// owns TMEM and issues the MMAs. A gather lane keeps the source offsets of its
+// 32 rows of the tile in registers, so that its cp.async instructions issue
+// back to back (reading each offset from shared memory between them made the
+// gather issue-bound), and no gather lane waits for a TMA issue. The per-expert pair counts are prefix-summed in shared memory
 // from expert_offsets at kernel start.
 #include "common.cuh"
 #include "ptx.cuh"
@@ -35,23 +51,25 @@
 
 namespace moe {
 
-bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
+bool make_tmap_bf16_2d_k32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
 
 namespace pair {
 
 constexpr int kHalf = 128;
 constexpr int kBN = 256;
-constexpr int kBK = 64;
-constexpr int kStages = 3;
+constexpr int kBK = 32;  // one 64-byte swizzle row of bf16
+constexpr int kStages = 6;
 constexpr int kHalfBytes = kHalf * kBK * 2;
 constexpr int kABytes = 2 * kHalfBytes;
 constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each draining half of the column chunks
 constexpr int kTmaWarp = kEpiWarps;
 constexpr int kGatherWarp0 = kEpiWarps + 1;
-constexpr int kMmaWarp = kGatherWarp0 + 2 * kStages;
+constexpr int kMmaWarp = kGatherWarp0 + kStages;  // one gather warp per ring slot
 constexpr int kGemmThreads = 32 * (kMmaWarp + 1);
 constexpr int kTmemCols = 2 * kBN;
+constexpr int kQ = 4;                                        // claimed-tile queue entries
+constexpr int kQConsumers = kStages + 1 + kEpiWarps;          // gather warps, MMA thread, epilogue warps
 constexpr int kStagePitch = 18;  // 32-bit words per staged row: 16 bf16 pairs, 8-byte aligned rows
 constexpr size_t kCtlBytes = 256 + 4 * (MOE_MAX_EXPERTS + 1) + 12 + kEpiWarps * 32 * kStagePitch * 4;
 constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + kCtlBytes;
@@ -69,6 +87,7 @@ struct GemmArgs {
   int b_rows_per_expert;
   float4* clear;    // fp32 accumulator of the down pass to zero (null: none)
   size_t clear_n4;  // its length in float4
+  int* tile_counter;  // tiles claimed beyond the first gridDim.x (zero at launch); null: fixed round-robin
 };
 
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
@@ -112,8 +131,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tfull_bar = bar_base + 8u * (2 * kStages);
   const uint32_t tempty_bar = bar_base + 8u * (2 * kStages + 1);
   const uint32_t done_bar = bar_base + 8u * (2 * kStages + 2);
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 128);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 132);
+  auto qfull_bar = [&](int q) { return bar_base + 8u * (2 * kStages + 3 + q); };
+  auto qempty_bar = [&](int q) { return bar_base + 8u * (2 * kStages + 3 + kQ + q); };
+  static_assert(8 * (2 * kStages + 3 + 2 * kQ) <= 192, "barriers overlap the control words");
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 196);
+  volatile int* tq = reinterpret_cast<volatile int*>(ctl + 208);  // [kQ] claimed tile ids
   int* pfx = reinterpret_cast<int*>(ctl + 256);
   float* stg_all = reinterpret_cast<float*>(pfx + (MOE_MAX_EXPERTS + 1) + 3);
 
@@ -123,12 +146,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(full_bar(s), 3);  // weight expect_tx arrive + one arrive per gather warp
+      ptx::mbar_init(full_bar(s), 2);  // weight expect_tx arrive + the slot's gather warp
       ptx::mbar_init(empty_bar(s), 1);
     }
     ptx::mbar_init(tfull_bar, 1);
     ptx::mbar_init(tempty_bar, 32 * kEpiWarps);
     ptx::mbar_init(done_bar, 1);
+    for (int q = 0; q < kQ; ++q) {
+      ptx::mbar_init(qfull_bar(q), 1);
+      ptx::mbar_init(qempty_bar(q), kQConsumers);
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -171,17 +198,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int tiles = pfx[args.E] * args.n_tiles;
-  const int kblocks = args.K / kBK;
+  const int kblocks = args.K / kBK;  // >= kStages (the host requires K >= 256)
+  // The next tile is claimed, and read by the gather warps for their token
+  // prefetch, from this K step of the current tile on.
+  const int claim_at = kblocks > 2 * kStages ? kblocks - 2 * kStages : 0;
+
+  // Queue entry j (the CTA's j-th tile): read once by every consumer warp (all
+  // its lanes, warp_wide) or by the single MMA thread.
+  auto read_tile = [&](int j, int& t_out, bool warp_wide) -> bool {
+    const int q = j % kQ;
+    const bool ok = ptx::mbar_wait(qfull_bar(q), static_cast<uint32_t>(j / kQ) & 1u, abort_flag);
+    t_out = ok ? tq[q] : tiles;
+    if (warp_wide) __syncwarp();
+    if (ok && (!warp_wide || lane == 0)) ptx::mbar_arrive(qempty_bar(q));
+    return ok;
+  };
 
   if (warp == kTmaWarp) {
     if (lane == 0) {
       int stage = 0, issued = 0;
       uint32_t phase = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      auto publish = [&](int j, int t) -> bool {
+        const int q = j % kQ;
+        if (!ptx::mbar_wait(qempty_bar(q), (static_cast<uint32_t>(j / kQ) & 1u) ^ 1u, abort_flag)) return false;
+        tq[q] = t;
+        ptx::mbar_arrive(qfull_bar(q));  // release: the id is visible to the waiting consumers
+        return true;
+      };
+      int t = blockIdx.x;
+      bool ok = publish(0, t);
+      for (int j = 0; ok && t < tiles; ++j) {
         const TileInfo ti = decode_tile(pfx, args.offsets, args.E, args.n_tiles, t);
         const int b_row0 = ti.e * args.b_rows_per_expert + ti.nt * kHalf;
+        int t_next = tiles;
         for (int kb = 0; kb < kblocks; ++kb) {
+          if (kb == claim_at) {
+            t_next = args.tile_counter ? static_cast<int>(gridDim.x) + atomicAdd(args.tile_counter, 1)
+                                       : t + static_cast<int>(gridDim.x);
+            if (!publish(j + 1, t_next)) { ok = false; break; }
+          }
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t b_dst = sB + stage * kBBytes;
           ptx::mbar_arrive_expect_tx(full_bar(stage), kBBytes);
@@ -190,6 +245,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
+        t = t_next;
       }
 #pragma unroll
       for (int st = 0; st < kStages; ++st) {
@@ -199,50 +255,70 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     __syncwarp();
   } else if (warp >= kGatherWarp0 && warp < kMmaWarp) {
-    const int pw = warp - kGatherWarp0;
-    const int slot = pw >> 1;
-    const int half = pw & 1;
-    const uint32_t a_dst = sA + slot * kABytes + half * kHalfBytes;
-    const int chunk = lane & 7;
-    const int rsub = lane >> 3;
+    const int slot = warp - kGatherWarp0;
+    const uint32_t a_dst = sA + slot * kABytes;
+    const int chunk = lane & 3;  // 16-byte chunk of a 64-byte row
+    const int rsub = lane >> 2;  // row within an 8-row group
     const __nv_bfloat16* xc = args.x + chunk * 8;
-    // Token rows 4i + rsub of the half: offs holds the current tile's source
-    // offsets, pre the next tile's tokens, loaded while this tile streams.
-    int offs[kHalf / 4], pre[kHalf / 4];
-    int cached_t = -1, pre_t = -1;
-    bool present = false, pre_present = false;
-    auto load_toks = [&](int tt) {
-      const TileInfo tj = decode_tile(pfx, args.offsets, args.E, args.n_tiles, tt);
-      pre_present = half < tj.nblk;
-      const int32_t* toks = args.sorted_tok + tj.row0 + half * kHalf + rsub;
-#pragma unroll
-      for (int i = 0; i < kHalf / 4; ++i) pre[i] = pre_present ? __ldg(toks + 4 * i) : -1;
+    // Rows 8i + rsub of the tile (i < 16: first block, i >= 16: second): offs
+    // holds the current tile's source offsets, pre the next tile's tokens,
+    // loaded while this tile streams.
+    constexpr int kRows = 2 * kHalf / 8;
+    int offs[kRows], pre[kRows];
+    int cur_j = -1, pre_j = -1, pre_t = tiles;
+    int nblk = 0, pre_nblk = 0;
+    // Reads queue entry jj and loads that tile's token rows into pre[].
+    auto fetch = [&](int jj) -> bool {
+      int tt;
+      if (!read_tile(jj, tt, true)) return false;
+      pre_j = jj;
       pre_t = tt;
-    };
-    for (int g = slot;; g += kStages) {
-      const int t_local = g / kblocks;
-      const int t = blockIdx.x + t_local * gridDim.x;
-      if (t >= tiles) break;
-      const int kb = g - t_local * kblocks;
-      if (t != cached_t) {
-        if (pre_t != t) load_toks(t);
-        present = pre_present;
+      pre_nblk = 0;
+      if (tt < tiles) {
+        const TileInfo tj = decode_tile(pfx, args.offsets, args.E, args.n_tiles, tt);
+        pre_nblk = tj.nblk;
+        const int32_t* toks = args.sorted_tok + tj.row0 + rsub;
 #pragma unroll
-        for (int i = 0; i < kHalf / 4; ++i) offs[i] = pre[i] >= 0 ? pre[i] * args.K : -1;
-        cached_t = t;
-        if (t + static_cast<int>(gridDim.x) < tiles) load_toks(t + gridDim.x);
+        for (int i = 0; i < kRows; ++i) pre[i] = (i < kRows / 2 || tj.nblk == 2) ? __ldg(toks + 8 * i) : -1;
       }
+      return true;
+    };
+    // Every tile has kblocks >= kStages K steps, so this warp has at least one
+    // K step in every tile and in every tile's last 2 * kStages steps: it reads
+    // the queue entries in order, each exactly once.
+    for (int g = slot;; g += kStages) {
+      const int j = g / kblocks;
+      const int kb = g - j * kblocks;
+      if (j != cur_j) {
+        if (pre_j != j && !fetch(j)) break;
+        cur_j = j;
+        if (pre_t >= tiles) break;
+        nblk = pre_nblk;
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) offs[i] = pre[i] >= 0 ? pre[i] * args.K : -1;
+      }
+      if (kb >= claim_at && pre_j == j && !fetch(j + 1)) break;
       const uint32_t use = static_cast<uint32_t>(g / kStages);
       const bool ok = ptx::mbar_wait(empty_bar(slot), (use & 1u) ^ 1u, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
-      if (present) {
+      {
         const int k0 = kb * kBK;
+        // 64B swizzle: chunk c of row r at r * 64 + ((c ^ ((r >> 1) & 3)) << 4)
 #pragma unroll
-        for (int i = 0; i < kHalf / 4; ++i) {
-          const int r = i * 4 + rsub;
+        for (int i = 0; i < kRows / 2; ++i) {
+          const int r = i * 8 + rsub;
           const int off = offs[i];
-          const uint32_t dst = a_dst + r * 128 + ((chunk ^ (r & 7)) << 4);
+          const uint32_t dst = a_dst + r * 64 + ((chunk ^ ((r >> 1) & 3)) << 4);
           ptx::cp_async_16(dst, off >= 0 ? xc + off + k0 : args.x, off >= 0 ? 16u : 0u);
+        }
+        if (nblk == 2) {
+#pragma unroll
+          for (int i = kRows / 2; i < kRows; ++i) {
+            const int r = i * 8 + rsub;
+            const int off = offs[i];
+            const uint32_t dst = a_dst + r * 64 + ((chunk ^ ((r >> 1) & 3)) << 4);
+            ptx::cp_async_16(dst, off >= 0 ? xc + off + k0 : args.x, off >= 0 ? 16u : 0u);
+          }
         }
         ptx::cp_async_commit();
         ptx::cp_async_wait<0>();
@@ -257,18 +333,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(kHalf, kBN);
       int stage = 0;
       uint32_t phase = 0;
-      int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++it) {
+      for (int it = 0; ok; ++it) {
+        int t;
+        if (!read_tile(it, t, false) || t >= tiles) break;
         const TileInfo ti = decode_tile(pfx, args.offsets, args.E, args.n_tiles, t);
         if (!ptx::mbar_wait(tempty_bar, (static_cast<uint32_t>(it) & 1u) ^ 1u, abort_flag)) break;
         ptx::tc_fence_after();
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint64_t a0 = ptx::sdesc_sw128(sA + stage * kABytes);
-          const uint64_t a1 = ptx::sdesc_sw128(sA + stage * kABytes + kHalfBytes);
-          const uint64_t bd = ptx::sdesc_sw128(sB + stage * kBBytes);
+          const uint64_t a0 = ptx::sdesc_sw64(sA + stage * kABytes);
+          const uint64_t a1 = ptx::sdesc_sw64(sA + stage * kABytes + kHalfBytes);
+          const uint64_t bd = ptx::sdesc_sw64(sB + stage * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             ptx::mma_f16(tmem_base, a0 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
@@ -296,8 +373,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const size_t hi = lo + per < args.clear_n4 ? lo + per : args.clear_n4;
       for (size_t i = lo + tid; i < hi; i += 32 * kEpiWarps) args.clear[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    int it = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+    for (int it = 0;; ++it) {
+      int t;
+      if (!read_tile(it, t, true) || t >= tiles) break;
       const TileInfo ti = decode_tile(pfx, args.offsets, args.E, args.n_tiles, t);
       if (!ptx::mbar_wait(tfull_bar, static_cast<uint32_t>(it) & 1u, abort_flag)) break;
       ptx::tc_fence_after();
@@ -348,16 +426,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 moe_status_t launch_gemm_gate_up_pairs(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_tok,
                                        const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
-                                       int H, int I, int E, float* y_clear, size_t y_clear_floats, cudaStream_t s) {
+                                       int H, int I, int E, float* y_clear, size_t y_clear_floats,
+                                       int* tile_counter, cudaStream_t s) {
   (void)num_pairs; (void)topk;
+  if (H < pair::kStages * pair::kBK) return MOE_ERR_UNSUPPORTED;
   using namespace pair;
   CUtensorMap map_b;
-  if (!make_tmap_bf16_2d(&map_b, w1, static_cast<uint64_t>(E) * 2 * I, H)) return MOE_ERR_CUDA;
+  if (!make_tmap_bf16_2d_k32(&map_b, w1, static_cast<uint64_t>(E) * 2 * I, H)) return MOE_ERR_CUDA;
   GemmArgs a{};
   a.x = x; a.sorted_tok = sorted_tok; a.offsets = offsets; a.h = h; a.err = err;
   a.E = E; a.K = H; a.I = I;
   a.n_tiles = I / kHalf; a.b_rows_per_expert = 2 * I;
   a.clear = reinterpret_cast<float4*>(y_clear); a.clear_n4 = y_clear ? y_clear_floats / 4 : 0;
+  a.tile_counter = tile_counter;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_gate_up_kernel), static_cast<int>(kGemmSmem)))
     return MOE_ERR_CUDA;
   moe_gate_up_kernel<<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_b, a);

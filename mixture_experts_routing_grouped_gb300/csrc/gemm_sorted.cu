@@ -284,6 +284,20 @@ bool make_tmap_bf16_2d_rows(CUtensorMap* map, const void* base, uint64_t rows, u
   return r == CUDA_SUCCESS;
 }
 
+// Same with a box of 32 columns (64 bytes) x 128 rows and 64B swizzle.
+bool make_tmap_bf16_2d_k32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+  auto encode = get_encode_fn();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kBM)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2D 8-bit tensor map over a row-major [rows, cols] byte matrix, box = 128 x 128,
 // 128B swizzle (tcgen05 operand) or none (staging read back by threads).
 bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, bool swizzle128) {

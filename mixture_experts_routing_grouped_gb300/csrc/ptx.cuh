@@ -300,6 +300,18 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 // 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked
 // along M/N (stride byte offset 1024). The tile base must be 1024-byte aligned;
 // stepping K by 16 bf16 (32 bytes) inside the atom adds 2 to the address field.
+// K-major operand tile of 64-byte rows (32 bf16) in the 64B-swizzled layout
+// that a TMA load with CU_TENSOR_MAP_SWIZZLE_64B writes: 16-byte chunk c of row r
+// sits at r * 64 + ((c ^ ((r >> 1) & 3)) << 4); 8-row groups are 512 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);    // start address
+  d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused for swizzled K-major)
+  d |= static_cast<uint64_t>(512 >> 4) << 32;            // stride byte offset: next 8-row group
+  d |= static_cast<uint64_t>(1) << 46;                   // descriptor version (tcgen05)
+  d |= static_cast<uint64_t>(4) << 61;                   // swizzle: 64B
+  return d;
+}
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);    // start address
