@@ -62,7 +62,7 @@ class ClockSampler:
             self.path.parent.mkdir(exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "10"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -283,6 +283,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
         "clocks": clk,
     }
     if not args.skip_extra and world == 1:
+        result["cublas_context"] = bench_cublas_context(torch, dev, flush, cfg, ids, args)
         result["decode"] = bench_decode(moe, synth, torch, dev, flush, peaks, args)
         result["routing"] = bench_routing(moe, synth, torch, dev, flush, peaks, args)
         result["gmm_lowp"] = bench_lowp(moe, synth, torch, dev, flush, peaks, args)
@@ -373,8 +374,55 @@ def bench_routing(moe, synth, torch, dev, flush, peaks, args):
         us = statistics.median(times) * 1e3
         nbytes = T * cfg.E * 4 + T * cfg.topk * 8
         gbs = nbytes / (us * 1e-6) / 1e9
+        # context: a plain one-pass read of the same logits (row maxima by torch) timed the same way
+        mx = torch.empty((T,), dtype=torch.float32, device=dev)
+        floor = []
+        for k in range(max(10, args.steps)):
+            flush(k)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            torch.amax(g, dim=1, out=mx)
+            b.record()
+            b.synchronize()
+            floor.append(a.elapsed_time(b))
+        floor_us = statistics.median(floor) * 1e3
         out[f"T{T}"] = {"us": round(us, 2), "bytes": nbytes, "GB/s": round(gbs, 1),
-                        "frac_hbm": round(gbs / float(peaks["hbm_gbs"]), 4)}
+                        "frac_hbm": round(gbs / float(peaks["hbm_gbs"]), 4),
+                        "read_floor_us": round(floor_us, 2),
+                        "read_floor_note": "torch.amax over the same [T, E] fp32 logits, one pass, same L2 flush"}
+    return out
+
+
+def bench_cublas_context(torch, dev, flush, cfg, ids, args):
+    """Context for the grouped GEMMs: cuBLAS batched GEMMs (torch.bmm) on the same per-expert shapes,
+    without the row gather, the SwiGLU and the weighted combine, with every expert holding the same
+    number of rows: T*k/E (the routed rows) and the padded row count the grouped kernels execute."""
+    import numpy as np
+    counts = np.bincount(ids.reshape(-1).cpu().numpy(), minlength=cfg.E)
+    padded = int(((counts + 127) // 128 * 128).sum())
+    out = {}
+    for rows, tag in ((cfg.T * cfg.topk // cfg.E, "routed"), (padded // cfg.E, "padded")):
+        for name, (kk, nn) in (("gate_up", (cfg.H, 2 * cfg.I)), ("down", (cfg.I, cfg.H))):
+            a = torch.randn(cfg.E, rows, kk, device=dev, dtype=torch.bfloat16)
+            b = torch.randn(cfg.E, kk, nn, device=dev, dtype=torch.bfloat16)
+            c = torch.empty(cfg.E, rows, nn, device=dev, dtype=torch.bfloat16)
+            for _ in range(3):
+                torch.bmm(a, b, out=c)
+            ts = []
+            for k in range(max(10, args.steps)):
+                flush(k)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                torch.bmm(a, b, out=c)
+                e1.record()
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            us = statistics.median(ts) * 1e3
+            useful = 2.0 * cfg.T * cfg.topk * kk * nn
+            out[f"{name}_{tag}"] = {"shape": f"bmm [{cfg.E}, {rows}, {kk}] x [{cfg.E}, {kk}, {nn}]", "us": round(us, 1),
+                                    "routed_TFLOP/s": round(useful / (us * 1e-6) / 1e12, 1)}
+            del a, b, c
+    torch.cuda.empty_cache()
     return out
 
 
