@@ -13,7 +13,9 @@ pages it cites:
 * ``align``    ``moe_align_block_size`` (mini-sglang MoE chapter, "fused MoE");
 * ``moe``      the expert-loop MoE forward (mini-sglang ``TorchMoeBackend``),
   the token-view form and the per-pair gathered projection (Fused MoE Part 3,
-  sections 01 and 03);
+  sections 01 and 03), and the layer with FP8-e4m3 GEMM operands (per-token
+  activation and per-channel weight scales, low-precision GMM article,
+  sections 2.3, 3.2 and 4.3);
 * ``quant``    symmetric per-row INT8 / FP8-e4m3 quantisation (low-precision
   GMM article, section 3.2) and the OCP E4M3 code book;
 * ``gmm``      the dequantise-then-matmul grouped GEMM (low-precision GMM

@@ -118,3 +118,54 @@ def token_outputs(x_rows, w1_experts, w2_experts, weights) -> np.ndarray:
         h = silu(w1e[:I] @ x) * (w1e[I:] @ x)
         out = out + float(wj) * (np.asarray(w2e, dtype=np.float64) @ h)
     return out
+
+
+def _bf16_round(v: np.ndarray) -> np.ndarray:
+    """float64 -> float32 -> bfloat16 (round to nearest even) -> float64."""
+    import torch
+    t = torch.from_numpy(np.asarray(v, dtype=np.float32))
+    return t.to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def fused_forward_fp8(x, gating_output, qw1, sw1, qw2, sw2, topk: int, renormalize: bool,
+                      num_expert_group: int = 1, topk_group: int = 1, scoring_func: str = "softmax",
+                      routed_scaling_factor: float = 1.0):
+    """The layer with FP8-e4m3 GEMM operands (low-precision GMM article: sections 2.3, 3.1, 3.2, 4.3).
+
+    Per the article, weights carry one scale per output channel, activations one
+    scale per token computed from the activation itself, products accumulate at
+    full precision and only the operands of the matrix instructions are 8-bit:
+
+    1. routing as in ``fused_forward``;
+    2. ``(qx, sx) = quant_rows_e4m3(x)`` (one scale per token);
+    3. for every (token t, slot j) pair with expert e:
+       ``g = sx[t] * sw1[e, :I] * (deq(qx[t]) @ deq(qw1[e, :I])^T)``, ``u`` likewise
+       with rows ``[I, 2I)``; ``h = silu(g) * u`` (float64);
+    4. ``h`` is held in the layer's activation dtype (rounded to bfloat16) and
+       quantised per pair row: ``(qh, sh) = quant_rows_e4m3(h)``;
+    5. ``y[t] += w[t, j] * sh * sw2[e] * (deq(qh) @ deq(qw2[e])^T)``.
+
+    ``qw1`` uint8 e4m3 codes [E, 2I, H] with ``sw1`` [E, 2I]; ``qw2`` [E, H, I] with
+    ``sw2`` [E, H]. Returns (y float64 [T, H], topk_weights float32, topk_ids int32).
+    """
+    from . import quant
+    tw, ids = routing.grouped_topk(gating_output, topk, renormalize, num_expert_group,
+                                   topk_group, scoring_func, routed_scaling_factor)
+    x = np.asarray(x, dtype=np.float32)
+    qx, sx = quant.quant_rows_e4m3(x)
+    dx = quant.dequant(qx, "e4m3") * sx.astype(np.float64)[:, None]        # sx[t] * deq(qx[t])
+    w1 = quant.dequant(qw1, "e4m3") * np.asarray(sw1, dtype=np.float64)[:, :, None]
+    w2 = quant.dequant(qw2, "e4m3") * np.asarray(sw2, dtype=np.float64)[:, :, None]
+    I = w1.shape[1] // 2
+    T, k = ids.shape
+    y = np.zeros((T, w2.shape[1]))
+    for t in range(T):
+        for j in range(k):
+            e = ids[t, j]
+            g = w1[e, :I] @ dx[t]
+            u = w1[e, I:] @ dx[t]
+            h = _bf16_round(silu(g) * u)
+            qh, sh = quant.quant_rows_e4m3(h[None, :])
+            dh = quant.dequant(qh[0], "e4m3") * float(sh[0])
+            y[t] += float(tw[t, j]) * (w2[e] @ dh)
+    return y, tw, ids
