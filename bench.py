@@ -284,6 +284,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
     }
     if not args.skip_extra and world == 1:
         result["cublas_context"] = bench_cublas_context(torch, dev, flush, cfg, ids, args)
+        result["fp8_layer"] = bench_fp8_layer(moe, torch, dev, flush, peaks, args, cfg, acts, W)
         result["decode"] = bench_decode(moe, synth, torch, dev, flush, peaks, args)
         result["routing"] = bench_routing(moe, synth, torch, dev, flush, peaks, args)
         result["gmm_lowp"] = bench_lowp(moe, synth, torch, dev, flush, peaks, args)
@@ -391,6 +392,65 @@ def bench_routing(moe, synth, torch, dev, flush, peaks, args):
                         "read_floor_us": round(floor_us, 2),
                         "read_floor_note": "torch.amax over the same [T, E] fp32 logits, one pass, same L2 flush"}
     return out
+
+
+def bench_fp8_layer(moe, torch, dev, flush, peaks, args, cfg, acts, W):
+    """The prefill layer with FP8-e4m3 weights (per-channel scales, quantised once by the library)
+    and per-token quantised activations: moe_fused_forward_fp8, device-timed like the bf16 layer."""
+    E, I, H = cfg.E, cfg.I, cfg.H
+    q1, s1 = moe.moe_quant_per_token(W["w1"].view(E * 2 * I, H), torch.float8_e4m3fn)
+    q2, s2 = moe.moe_quant_per_token(W["w2"].view(E * H, I), torch.float8_e4m3fn)
+    q1, s1, q2, s2 = q1.view(E, 2 * I, H), s1.view(E, 2 * I), q2.view(E, H, I), s2.view(E, H)
+    ws = torch.zeros(moe.moe_fused_forward_fp8_workspace_size(cfg.T, H, I, E, cfg.topk), dtype=torch.uint8,
+                     device=dev)
+    y = torch.empty((cfg.T, H), dtype=torch.bfloat16, device=dev)
+    tw = torch.empty((cfg.T, cfg.topk), dtype=torch.float32, device=dev)
+    ids = torch.empty((cfg.T, cfg.topk), dtype=torch.int32, device=dev)
+    run = lambda: moe.moe_fused_forward_fp8(acts["x"], acts["gating"], q1, s1, q2, s2, cfg.topk, cfg.renormalize,
+                                            cfg.num_expert_group, cfg.topk_group, cfg.scoring,
+                                            cfg.routed_scaling_factor, ws=ws, y=y, topk_weights=tw, topk_ids=ids)
+    for _ in range(args.warmup):
+        run()
+    K = max(10, args.steps)
+    times = []
+    for k in range(K):
+        flush(k)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        run()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    n_ev = 8
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K)]
+    for row in ev:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    for k in range(K):
+        flush(k)
+        moe.moe_set_stage_events(ev[k])
+        run()
+        moe.moe_set_stage_events(None)
+    torch.cuda.synchronize()
+    names = ["routing", "align", "quant_x", "gemm_gate_up", "quant_h", "gemm_down", "cast"]
+    stage = {n: statistics.median(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K)) for i, n in enumerate(names)}
+    if moe.moe_check_device_error(ws):
+        raise RuntimeError("moe_fused_forward_fp8 reported a device error")
+    ms = statistics.median(times)
+    pairs = cfg.T * cfg.topk
+    f_gu, f_dn = 2.0 * pairs * H * 2 * I, 2.0 * pairs * I * H
+    peak8 = 2.0 * float(peaks["bf16_tflops"])
+    gu_tf = f_gu / (stage["gemm_gate_up"] * 1e-3) / 1e12
+    dn_tf = f_dn / (stage["gemm_down"] * 1e-3) / 1e12
+    return {"workload": cfg.name + "_fp8_e4m3", "ms_per_step": round(ms, 4),
+            "tokens/s": round(cfg.T / (ms * 1e-3), 1),
+            "layer_TFLOP/s": round((f_gu + f_dn) / (ms * 1e-3) / 1e12, 1),
+            "stage_ms": {k: round(v, 4) for k, v in stage.items()},
+            "gate_up_TFLOP/s": round(gu_tf, 1), "down_TFLOP/s": round(dn_tf, 1),
+            "fp8_peak_TFLOP/s": peak8, "gate_up_frac_fp8_peak": round(gu_tf / peak8, 4),
+            "peak_source": "2 x bf16_tflops (burst) of measured: the nominal fp8 / bf16 dense ratio",
+            "gpu_launches_per_step": 8}
 
 
 def bench_cublas_context(torch, dev, flush, cfg, ids, args):

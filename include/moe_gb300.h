@@ -148,6 +148,40 @@ MOE_API moe_status_t moe_fused_forward(const void* x, const float* gating, const
                                size_t ws_bytes, void* stream);
 
 /*
+ * moe_fused_forward_fp8 -- the same layer with FP8-e4m3 GEMM operands.
+ * Defined by the low-precision GMM article (pwwt.cn): section 2.3 (weights with one
+ * scale per output channel, activations with one scale per token computed from the
+ * activation itself, fp32 accumulation, 8-bit values only as the matrix
+ * instructions' operands), section 3.2 (symmetric scales, absmax / 448 for FP8) and
+ * section 4.3 (gate and up share one epilogue whose output feeds the next GEMM);
+ * the layer around it is that of moe_fused_forward. Steps, all on the device:
+ * routing; align; x quantised per token to e4m3 (scale sx[t]); gate_up on the
+ * gathered code rows with g = sx[t] * sw1[e, n] * acc, u likewise, h = silu(g) * u
+ * held in bf16; h quantised per row to e4m3 (scale sh[row]); down with
+ * y[t] += w[t, j] * sh[row] * sw2[e, n] * acc; cast of y to bf16.
+ *
+ *  x                [T, H] bf16 hidden states (quantised inside the call).
+ *  gating           [T, E] fp32 router logits.
+ *  w_gate_up        [E, 2I, H] e4m3 codes (one byte each, OCP E4M3), K-major; rows
+ *                   [0, I) gate, [I, 2I) up.
+ *  scales_gate_up   [E, 2I] fp32 per-output-channel scales (16-byte aligned).
+ *  w_down           [E, H, I] e4m3 codes, K-major.
+ *  scales_down      [E, H] fp32 per-output-channel scales (16-byte aligned).
+ *  Other arguments, outputs and conditions as for moe_fused_forward (H a multiple of
+ *  256, I a multiple of 128); ws of at least moe_fused_forward_fp8_workspace_size(...)
+ *  bytes, 256-byte aligned and zero-filled before its first use. Every problem size
+ *  uses the 128-row block layout (no decode-specific kernel for this dtype).
+ */
+MOE_API size_t moe_fused_forward_fp8_workspace_size(int T, int H, int I, int E, int topk);
+MOE_API moe_status_t moe_fused_forward_fp8(const void* x, const float* gating, const void* w_gate_up,
+                                           const float* scales_gate_up, const void* w_down,
+                                           const float* scales_down, int T, int H, int I, int E,
+                                           int num_expert_group, int topk_group, int topk, int scoring,
+                                           int renormalize, float routed_scaling_factor, void* y,
+                                           float* topk_weights, int32_t* topk_ids, void* ws,
+                                           size_t ws_bytes, void* stream);
+
+/*
  * moe_fused_forward_noalloc -- moe_fused_forward without a caller-provided workspace.
  * The pages have no counterpart: this entry point exists for callers that cannot
  * allocate device memory (a plug-in or backend inside a host framework that owns
@@ -184,8 +218,10 @@ MOE_API moe_status_t moe_fused_forward_noalloc(const void* x, const float* gatin
  * kernel and events[i] after its i-th step: 1 routing, 2 align, 3 gate_up GEMM,
  * 4 down GEMM, 5 cast to bf16 (n >= 6 records all). The fp32 accumulator of the
  * down pass is cleared inside step 3 (prefill kernels) or step 1 (decode
- * kernels). The events are cudaEvent_t handles owned by the caller. events =
- * NULL or n = 0 switches the recording off.
+ * kernels). moe_fused_forward_fp8 records events[0] before routing and after
+ * 1 routing, 2 align, 3 quantisation of x, 4 gate_up GEMM, 5 quantisation of h,
+ * 6 down GEMM, 7 cast (n = 8 records all). The events are cudaEvent_t handles
+ * owned by the caller. events = NULL or n = 0 switches the recording off.
  */
 MOE_API void moe_set_stage_events(void* const* events, int n);
 

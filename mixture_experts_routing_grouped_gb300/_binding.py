@@ -30,6 +30,9 @@ _SIGNATURES = {
     "moe_fused_forward_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "moe_fused_forward": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                    _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp, _c_size, _vp]),
+    "moe_fused_forward_fp8_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "moe_fused_forward_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                       _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "moe_fused_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                            _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp]),
     "moe_quant_per_token": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
@@ -177,6 +180,47 @@ def moe_fused_forward(x: torch.Tensor, gating: torch.Tensor, w_gate_up: torch.Te
                                  float(routed_scaling_factor), _ptr(y), _ptr(topk_weights), _ptr(topk_ids),
                                  _ptr(ws), ws.numel(), _stream(x))
     _check("moe_fused_forward", st)
+    return y, topk_weights, topk_ids
+
+
+def moe_fused_forward_fp8_workspace_size(T: int, H: int, I: int, E: int, topk: int) -> int:
+    return int(lib().moe_fused_forward_fp8_workspace_size(T, H, I, E, topk))
+
+
+def moe_fused_forward_fp8(x: torch.Tensor, gating: torch.Tensor, w_gate_up: torch.Tensor,
+                          scales_gate_up: torch.Tensor, w_down: torch.Tensor, scales_down: torch.Tensor, topk: int,
+                          renormalize: bool = True, num_expert_group: int = 1, topk_group: int = 1,
+                          scoring_func: str = "softmax", routed_scaling_factor: float = 1.0,
+                          ws: torch.Tensor | None = None, y: torch.Tensor | None = None,
+                          topk_weights: torch.Tensor | None = None, topk_ids: torch.Tensor | None = None):
+    """The routed MoE layer with e4m3 weights (codes as torch.float8_e4m3fn or uint8) and fp32
+    per-channel scales: returns (y bf16 [T, H], topk_weights fp32 [T, k], topk_ids int32 [T, k])."""
+    _need(x, "x", torch.bfloat16)
+    T, H = x.shape
+    E, I2, H2 = w_gate_up.shape
+    I = I2 // 2
+    for t, name, shape in ((w_gate_up, "w_gate_up", (E, 2 * I, H)), (w_down, "w_down", (E, H, I))):
+        if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise TypeError(f"{name} must hold e4m3 codes (torch.float8_e4m3fn or uint8), got {t.dtype}")
+        _need(t, name, None, shape)
+    _need(gating, "gating", torch.float32, (T, E))
+    _need(scales_gate_up, "scales_gate_up", torch.float32, (E, 2 * I))
+    _need(scales_down, "scales_down", torch.float32, (E, H))
+    dev = x.device
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty((T, topk), dtype=torch.float32, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    wsb = moe_fused_forward_fp8_workspace_size(T, H, I, E, topk)
+    if ws is None:
+        ws = torch.zeros(max(wsb, 256), dtype=torch.uint8, device=dev)
+    st = lib().moe_fused_forward_fp8(_ptr(x), _ptr(gating), _ptr(w_gate_up), _ptr(scales_gate_up), _ptr(w_down),
+                                     _ptr(scales_down), T, H, I, E, num_expert_group, topk_group, topk,
+                                     SCORING[scoring_func], int(bool(renormalize)), float(routed_scaling_factor),
+                                     _ptr(y), _ptr(topk_weights), _ptr(topk_ids), _ptr(ws), ws.numel(), _stream(x))
+    _check("moe_fused_forward_fp8", st)
     return y, topk_weights, topk_ids
 
 

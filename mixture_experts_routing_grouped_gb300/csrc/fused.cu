@@ -43,6 +43,17 @@ moe_status_t launch_gemm_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, c
                               const int32_t* expert_ids, const int32_t* ntpp, const float* topk_w, float* y_acc,
                               int* err, int num_pairs, int topk, int cap, int H, int I, int E, cudaStream_t s);
 
+moe_status_t launch_gemm_gate_up_pairs_fp8(const uint8_t* qx, const float* sx, const uint8_t* w1, const float* sw1,
+                                           const int32_t* sorted_tok, const int32_t* offsets, __nv_bfloat16* h,
+                                           int* err, int H, int I, int E, float* y_clear, size_t y_clear_floats,
+                                           int* tile_counter, cudaStream_t s);
+moe_status_t launch_gemm_down_fp8(const uint8_t* qh, const float* sh, const uint8_t* w2, const float* sw2,
+                                  const int32_t* sorted_ids, const int32_t* expert_ids, const int32_t* ntpp,
+                                  const float* topk_w, float* y_acc, int* err, int num_pairs, int topk, int cap,
+                                  int H, int I, int E, cudaStream_t s);
+moe_status_t launch_quant_rows_e4m3_bf16(const __nv_bfloat16* x, int M, int K, uint8_t* q, float* s,
+                                         const int* rows_dev, cudaStream_t st);
+
 moe_status_t launch_swap_gate_up(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_ids,
                                  const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk, int H,
                                  int I, int E, int nmax, cudaStream_t s);
@@ -125,6 +136,26 @@ FusedLayout fused_layout(int T, int H, int I, int E, int topk, int block_m) {
   L.ntpp = off; off = align_up(off + 4, 1024);
   L.h = off; off = align_up(off + static_cast<size_t>(L.cap) * I * 2, 1024);
   L.y_acc = off; off = align_up(off + static_cast<size_t>(T) * H * 4, 256);
+  L.total = off;
+  return L;
+}
+
+// The FP8 forward's workspace: the bf16 forward's 128-row layout, then the
+// per-token e4m3 codes of x and their scales, then the per-row e4m3 codes of h
+// and their scales.
+struct Fp8Layout {
+  FusedLayout base;
+  size_t qx, sx, qh, sh, total;
+};
+
+Fp8Layout fp8_layout(int T, int H, int I, int E, int topk) {
+  Fp8Layout L{};
+  L.base = fused_layout(T, H, I, E, topk, 128);
+  size_t off = align_up(L.base.total, 1024);
+  L.qx = off; off = align_up(off + static_cast<size_t>(T) * H, 1024);
+  L.sx = off; off = align_up(off + static_cast<size_t>(T) * 4, 1024);
+  L.qh = off; off = align_up(off + static_cast<size_t>(L.base.cap) * I, 1024);
+  L.sh = off; off = align_up(off + static_cast<size_t>(L.base.cap) * 4, 256);
   L.total = off;
   return L;
 }
@@ -234,5 +265,82 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
                                                     reinterpret_cast<uint2*>(y), n4);
   if ((st = launch_status()) != MOE_OK) return st;
   stage_mark(5, s);
+  return MOE_OK;
+}
+
+extern "C" size_t moe_fused_forward_fp8_workspace_size(int T, int H, int I, int E, int topk) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0) return 0;
+  return moe::fp8_layout(T, H, I, E, topk).total;
+}
+
+extern "C" moe_status_t moe_fused_forward_fp8(const void* x, const float* gating, const void* w_gate_up,
+                                              const float* scales_gate_up, const void* w_down,
+                                              const float* scales_down, int T, int H, int I, int E,
+                                              int num_expert_group, int topk_group, int topk, int scoring,
+                                              int renormalize, float routed_scaling_factor, void* y,
+                                              float* topk_weights, int32_t* topk_ids, void* ws, size_t ws_bytes,
+                                              void* stream) {
+  using namespace moe;
+  moe_status_t st = validate_routing(T, E, num_expert_group, topk_group, topk, scoring);
+  if (st != MOE_OK) return st;
+  if (H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+  if (!w_gate_up || !w_down || !scales_gate_up || !scales_down) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !gating || !y || !topk_weights || !topk_ids)) return MOE_ERR_INVALID_ARG;
+  if (H % 256 != 0 || I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(gating) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(y) ||
+      !aligned16(scales_gate_up) || !aligned16(scales_down))
+    return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (static_cast<long long>(T) * topk >= (1ll << 30) || static_cast<long long>(T) * H >= (1ll << 31))
+    return MOE_ERR_UNSUPPORTED;
+  const Fp8Layout L = fp8_layout(T, H, I, E, topk);
+  if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+
+  cudaStream_t s = as_stream(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* err = reinterpret_cast<int*>(w);
+  int* tile_counter = err + 1;  // gate_up tile claims: zeroed by the align step
+  int32_t* sorted_ids = reinterpret_cast<int32_t*>(w + L.base.sorted_ids);
+  int32_t* sorted_tok = reinterpret_cast<int32_t*>(w + L.base.sorted_tok);
+  int32_t* expert_ids = reinterpret_cast<int32_t*>(w + L.base.expert_ids);
+  int32_t* offsets = reinterpret_cast<int32_t*>(w + L.base.expert_offsets);
+  int32_t* ntpp = reinterpret_cast<int32_t*>(w + L.base.ntpp);
+  __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(w + L.base.h);
+  float* y_acc = reinterpret_cast<float*>(w + L.base.y_acc);
+  uint8_t* qx = w + L.qx;
+  float* sx = reinterpret_cast<float*>(w + L.sx);
+  uint8_t* qh = w + L.qh;
+  float* sh = reinterpret_cast<float*>(w + L.sh);
+  const int num_pairs = T * topk;
+  const int cap = L.base.cap;
+
+  stage_mark(0, s);
+  st = launch_grouped_topk(gating, T, E, num_expert_group, topk_group, topk, scoring, renormalize,
+                           routed_scaling_factor, topk_weights, topk_ids, s, nullptr, H, nullptr, 0);
+  if (st != MOE_OK) return st;
+  stage_mark(1, s);
+  st = launch_align(topk_ids, num_pairs, E, 128, sorted_ids, expert_ids, offsets, ntpp, w + L.base.align_scratch,
+                    err, s, sorted_tok, topk, tile_counter);
+  if (st != MOE_OK) return st;
+  stage_mark(2, s);
+  st = launch_quant_rows_e4m3_bf16(static_cast<const __nv_bfloat16*>(x), T, H, qx, sx, nullptr, s);
+  if (st != MOE_OK) return st;
+  stage_mark(3, s);
+  st = launch_gemm_gate_up_pairs_fp8(qx, sx, static_cast<const uint8_t*>(w_gate_up), scales_gate_up, sorted_tok,
+                                     offsets, h, err, H, I, E, y_acc, static_cast<size_t>(T) * H, tile_counter, s);
+  if (st != MOE_OK) return st;
+  stage_mark(4, s);
+  st = launch_quant_rows_e4m3_bf16(h, cap, I, qh, sh, ntpp, s);
+  if (st != MOE_OK) return st;
+  stage_mark(5, s);
+  st = launch_gemm_down_fp8(qh, sh, static_cast<const uint8_t*>(w_down), scales_down, sorted_ids, expert_ids, ntpp,
+                            topk_weights, y_acc, err, num_pairs, topk, cap, H, I, E, s);
+  if (st != MOE_OK) return st;
+  stage_mark(6, s);
+  const size_t n4 = static_cast<size_t>(T) * H / 4;
+  cast_f32_bf16_kernel<<<grid_for(n4), 256, 0, s>>>(reinterpret_cast<const float4*>(y_acc),
+                                                    reinterpret_cast<uint2*>(y), n4);
+  if ((st = launch_status()) != MOE_OK) return st;
+  stage_mark(7, s);
   return MOE_OK;
 }

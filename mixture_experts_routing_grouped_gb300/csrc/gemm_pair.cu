@@ -34,6 +34,14 @@
 // five K steps of MMA work queued against that, where three 64-column slots
 // left the MMA waiting for data for about 40 % of the kernel.
 //
+// The kernel is written in bytes of K: a K step is one 64-byte row segment of
+// both operands, 32 bf16 or 64 FP8-e4m3 values, and either way two MMAs of 32
+// bytes of K each (kind::f16 K=16, or kind::f8f6f4 K=32). The FP8 instance (the
+// low-precision GMM article's layer: per-token activation scales, per-channel
+// weight scales, fp32 accumulation, sections 2.3 and 4.3) gathers the rows of
+// the per-token-quantised activations and multiplies each accumulator by its
+// token's scale and its column's weight scale before the SwiGLU.
+//
 // Kernel shape (one persistent CTA per SM, 512 threads): warps 0-7 epilogue
 // (TMEM lane quarter = warp % 4, column chunks split between warps w and w+4, so
 // that the single accumulator is drained -- and the next tile's MMAs start --
@@ -52,16 +60,17 @@
 namespace moe {
 
 bool make_tmap_bf16_2d_k32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
+bool make_tmap_u8_2d_k64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
 
 namespace pair {
 
 constexpr int kHalf = 128;
 constexpr int kBN = 256;
-constexpr int kBK = 32;  // one 64-byte swizzle row of bf16
+constexpr int kKBytes = 64;  // bytes of K per step: one 64-byte swizzle row (32 bf16 or 64 e4m3)
 constexpr int kStages = 6;
-constexpr int kHalfBytes = kHalf * kBK * 2;
+constexpr int kHalfBytes = kHalf * kKBytes;
 constexpr int kABytes = 2 * kHalfBytes;
-constexpr int kBBytes = kBN * kBK * 2;
+constexpr int kBBytes = kBN * kKBytes;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each draining half of the column chunks
 constexpr int kTmaWarp = kEpiWarps;
 constexpr int kGatherWarp0 = kEpiWarps + 1;
@@ -75,13 +84,16 @@ constexpr size_t kCtlBytes = 256 + 4 * (MOE_MAX_EXPERTS + 1) + 12 + kEpiWarps * 
 constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + kCtlBytes;
 
 struct GemmArgs {
-  const __nv_bfloat16* x;
+  const uint8_t* x;           // activations [T, K] (bf16, or e4m3 codes), K contiguous
+  const float* sx;            // FP8: per-token activation scales [T]
+  const float* sw;            // FP8: per-channel weight scales [E, 2I]
   const int32_t* sorted_tok;  // token of each sorted row, -1 for padding
   const int32_t* offsets;
   __nv_bfloat16* h;
   int* err;
   int E;
-  int K;
+  int K;            // reduction length in elements
+  int row_bytes;    // bytes of one activation row
   int I;
   int n_tiles;
   int b_rows_per_expert;
@@ -116,8 +128,10 @@ __device__ __forceinline__ TileInfo decode_tile(const int* pfx, const int32_t* _
   return ti;
 }
 
+template <bool F8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gate_up_kernel(const __grid_constant__ CUtensorMap map_b, const GemmArgs args) {
+  constexpr int kElemsPerStep = F8 ? kKBytes : kKBytes / 2;  // K elements per step
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -198,7 +212,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int tiles = pfx[args.E] * args.n_tiles;
-  const int kblocks = args.K / kBK;  // >= kStages (the host requires K >= 256)
+  const int kblocks = args.K / kElemsPerStep;  // >= 1 (the host requires whole 64-byte steps)
   // The next tile is claimed, and read by the gather warps for their token
   // prefetch, from this K step of the current tile on.
   const int claim_at = kblocks > 2 * kStages ? kblocks - 2 * kStages : 0;
@@ -240,8 +254,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t b_dst = sB + stage * kBBytes;
           ptx::mbar_arrive_expect_tx(full_bar(stage), kBBytes);
-          ptx::tma_load_2d(b_dst, &map_b, full_bar(stage), kb * kBK, b_row0);
-          ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(stage), kb * kBK, b_row0 + args.I);
+          ptx::tma_load_2d(b_dst, &map_b, full_bar(stage), kb * kElemsPerStep, b_row0);
+          ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(stage), kb * kElemsPerStep, b_row0 + args.I);
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -259,7 +273,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t a_dst = sA + slot * kABytes;
     const int chunk = lane & 3;  // 16-byte chunk of a 64-byte row
     const int rsub = lane >> 2;  // row within an 8-row group
-    const __nv_bfloat16* xc = args.x + chunk * 8;
+    const uint8_t* xc = args.x + chunk * 16;
     // Rows 8i + rsub of the tile (i < 16: first block, i >= 16: second): offs
     // holds the current tile's source offsets, pre the next tile's tokens,
     // loaded while this tile streams.
@@ -283,26 +297,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       return true;
     };
-    // Every tile has kblocks >= kStages K steps, so this warp has at least one
-    // K step in every tile and in every tile's last 2 * kStages steps: it reads
-    // the queue entries in order, each exactly once.
+    // The warp reads the queue entries in order, each exactly once: at its first
+    // K step of tile j it reads any entries up to j that it has not read yet
+    // (tiles in which it has no K step when a tile has fewer K steps than the
+    // ring has slots), and it stops at the first entry past the last tile. When
+    // tiles have kblocks >= kStages steps it has a step in every tile and in
+    // every tile's last 2 * kStages steps, so the next tile's tokens are
+    // prefetched while the current one streams.
     for (int g = slot;; g += kStages) {
       const int j = g / kblocks;
       const int kb = g - j * kblocks;
       if (j != cur_j) {
-        if (pre_j != j && !fetch(j)) break;
+        // never read past the entry that ends the tiles: nothing is published after it
+        bool aborted = false;
+        while (pre_j < j && !(pre_j >= 0 && pre_t >= tiles)) {
+          if (!fetch(pre_j + 1)) { aborted = true; break; }
+        }
+        if (aborted || pre_t >= tiles) break;
         cur_j = j;
-        if (pre_t >= tiles) break;
         nblk = pre_nblk;
 #pragma unroll
-        for (int i = 0; i < kRows; ++i) offs[i] = pre[i] >= 0 ? pre[i] * args.K : -1;
+        for (int i = 0; i < kRows; ++i) offs[i] = pre[i] >= 0 ? pre[i] * args.row_bytes : -1;
       }
       if (kb >= claim_at && pre_j == j && !fetch(j + 1)) break;
       const uint32_t use = static_cast<uint32_t>(g / kStages);
       const bool ok = ptx::mbar_wait(empty_bar(slot), (use & 1u) ^ 1u, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       {
-        const int k0 = kb * kBK;
+        const int k0 = kb * kKBytes;
         // 64B swizzle: chunk c of row r at r * 64 + ((c ^ ((r >> 1) & 3)) << 4)
 #pragma unroll
         for (int i = 0; i < kRows / 2; ++i) {
@@ -330,7 +352,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ptx::cp_async_wait<0>();
   } else if (warp == kMmaWarp) {
     if (ptx::elect_one()) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kHalf, kBN);
+      constexpr uint32_t idesc = F8 ? ptx::idesc_e4m3_f32(kHalf, kBN) : ptx::idesc_bf16_f32(kHalf, kBN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -347,9 +369,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t a1 = ptx::sdesc_sw64(sA + stage * kABytes + kHalfBytes);
           const uint64_t bd = ptx::sdesc_sw64(sB + stage * kBBytes);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            ptx::mma_f16(tmem_base, a0 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
-            if (ti.nblk == 2) ptx::mma_f16(tmem_base + kBN, a1 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < kKBytes / 32; ++kk) {  // 32 bytes of K per MMA
+            if constexpr (F8) {
+              ptx::mma_f8(tmem_base, a0 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+              if (ti.nblk == 2) ptx::mma_f8(tmem_base + kBN, a1 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+            } else {
+              ptx::mma_f16(tmem_base, a0 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+              if (ti.nblk == 2) ptx::mma_f16(tmem_base + kBN, a1 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+            }
           }
           ptx::mma_commit(empty_bar(stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -383,12 +410,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int half = 0; half < ti.nblk; ++half) {
         const uint32_t tbase = tmem_base + lane_off + half * kBN;
         const int rowbase = ti.row0 + half * kHalf + quarter * 32;
+        float rs = 1.f;  // FP8: the row's token scale (0 for padding rows)
+        if constexpr (F8) {
+          const int tok = __ldg(args.sorted_tok + rowbase + lane);
+          rs = tok >= 0 ? __ldg(args.sx + tok) : 0.f;
+        }
 #pragma unroll 1
         for (int c = 2 * cpart; c < 2 * cpart + 2; ++c) {
           uint32_t g[32], u[32];
           ptx::tmem_ld32(tbase + c * 32, g);
           ptx::tmem_ld32(tbase + kHalf + c * 32, u);
           ptx::tmem_ld_wait();
+          if constexpr (F8) {
+            // g = sx[token] * sw[e, n] * acc_g, u = sx[token] * sw[e, I + n] * acc_u
+            const float* swg = args.sw + static_cast<size_t>(ti.e) * 2 * args.I + n0 + c * 32;
+            const float* swu = swg + args.I;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              const float4 a = __ldg(reinterpret_cast<const float4*>(swg + j));
+              const float4 b = __ldg(reinterpret_cast<const float4*>(swu + j));
+              g[j] = __float_as_uint(rs * a.x * __uint_as_float(g[j]));
+              g[j + 1] = __float_as_uint(rs * a.y * __uint_as_float(g[j + 1]));
+              g[j + 2] = __float_as_uint(rs * a.z * __uint_as_float(g[j + 2]));
+              g[j + 3] = __float_as_uint(rs * a.w * __uint_as_float(g[j + 3]));
+              u[j] = __float_as_uint(rs * b.x * __uint_as_float(u[j]));
+              u[j + 1] = __float_as_uint(rs * b.y * __uint_as_float(u[j + 1]));
+              u[j + 2] = __float_as_uint(rs * b.z * __uint_as_float(u[j + 2]));
+              u[j + 3] = __float_as_uint(rs * b.w * __uint_as_float(u[j + 3]));
+            }
+          }
           uint32_t* srow = reinterpret_cast<uint32_t*>(stg + lane * kStagePitch);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -424,25 +474,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 }  // namespace pair
 
+namespace {
+
+template <bool F8>
+moe_status_t launch_gate_up(const CUtensorMap& map_b, const pair::GemmArgs& a, cudaStream_t s) {
+  using namespace pair;
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_gate_up_kernel<F8>), static_cast<int>(kGemmSmem)))
+    return MOE_ERR_CUDA;
+  moe_gate_up_kernel<F8><<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_b, a);
+  return launch_status();
+}
+
+}  // namespace
+
 moe_status_t launch_gemm_gate_up_pairs(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_tok,
                                        const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
                                        int H, int I, int E, float* y_clear, size_t y_clear_floats,
                                        int* tile_counter, cudaStream_t s) {
   (void)num_pairs; (void)topk;
-  if (H < pair::kStages * pair::kBK) return MOE_ERR_UNSUPPORTED;
   using namespace pair;
+  if ((H * 2) % kKBytes != 0) return MOE_ERR_UNSUPPORTED;
   CUtensorMap map_b;
   if (!make_tmap_bf16_2d_k32(&map_b, w1, static_cast<uint64_t>(E) * 2 * I, H)) return MOE_ERR_CUDA;
   GemmArgs a{};
-  a.x = x; a.sorted_tok = sorted_tok; a.offsets = offsets; a.h = h; a.err = err;
-  a.E = E; a.K = H; a.I = I;
+  a.x = reinterpret_cast<const uint8_t*>(x); a.sorted_tok = sorted_tok; a.offsets = offsets; a.h = h; a.err = err;
+  a.E = E; a.K = H; a.row_bytes = H * 2; a.I = I;
   a.n_tiles = I / kHalf; a.b_rows_per_expert = 2 * I;
   a.clear = reinterpret_cast<float4*>(y_clear); a.clear_n4 = y_clear ? y_clear_floats / 4 : 0;
   a.tile_counter = tile_counter;
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_gate_up_kernel), static_cast<int>(kGemmSmem)))
-    return MOE_ERR_CUDA;
-  moe_gate_up_kernel<<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_b, a);
-  return launch_status();
+  return launch_gate_up<false>(map_b, a, s);
+}
+
+moe_status_t launch_gemm_gate_up_pairs_fp8(const uint8_t* qx, const float* sx, const uint8_t* w1, const float* sw1,
+                                           const int32_t* sorted_tok, const int32_t* offsets, __nv_bfloat16* h,
+                                           int* err, int H, int I, int E, float* y_clear, size_t y_clear_floats,
+                                           int* tile_counter, cudaStream_t s) {
+  using namespace pair;
+  if (H % kKBytes != 0) return MOE_ERR_UNSUPPORTED;
+  CUtensorMap map_b;
+  if (!make_tmap_u8_2d_k64(&map_b, w1, static_cast<uint64_t>(E) * 2 * I, H)) return MOE_ERR_CUDA;
+  GemmArgs a{};
+  a.x = qx; a.sx = sx; a.sw = sw1; a.sorted_tok = sorted_tok; a.offsets = offsets; a.h = h; a.err = err;
+  a.E = E; a.K = H; a.row_bytes = H; a.I = I;
+  a.n_tiles = I / kHalf; a.b_rows_per_expert = 2 * I;
+  a.clear = reinterpret_cast<float4*>(y_clear); a.clear_n4 = y_clear ? y_clear_floats / 4 : 0;
+  a.tile_counter = tile_counter;
+  return launch_gate_up<true>(map_b, a, s);
 }
 
 }  // namespace moe

@@ -10,12 +10,21 @@
 // accumulator. h is contiguous per expert (the gate_up kernels write it in
 // sorted order), so both operands arrive by TMA.
 //
-// Kernel shape (one persistent CTA per SM, 192 threads):
-//   warps 0-3  epilogue: TMEM -> registers -> shared staging -> fp32 atomics
-//              (TMEM lane quarter = warp)
-//   warp 4     one thread sends A and B of every K step by TMA through the
+// Kernel shape (one persistent CTA per SM, 320 threads):
+//   warps 0-7  epilogue: TMEM -> registers -> shared staging -> fp32 atomics
+//              (TMEM lane quarter = warp % 4, column half = warp / 4: two warps
+//              drain each accumulator row, so that the combine of a tile stays
+//              shorter than the main loop of the next when K is short, as with
+//              FP8 operands)
+//   warp 8     one thread sends A and B of every K step by TMA through the
 //              4-slot ring
-//   warp 5     TMEM allocation and the single MMA-issuing thread
+//   warp 9     TMEM allocation and the single MMA-issuing thread
+// The kernel is written in bytes of K: a K step is one 128-byte swizzle row of
+// both operands (64 bf16 or 128 FP8-e4m3 values), four MMAs of 32 bytes of K.
+// The FP8 instance (the low-precision GMM article's layer: per-token
+// activation scales, per-channel weight scales, sections 2.3 and 4.3) reads h
+// quantised per row and multiplies each accumulator by its row's scale and its
+// column's weight scale in the epilogue, together with the route weight.
 // The 128 x 256 fp32 accumulator lives in TMEM, double-buffered (512 columns)
 // so that the combine of one tile overlaps the main loop of the next.
 // Tiles (m-block, n-block) are taken round-robin with the n-block fastest, so
@@ -35,13 +44,15 @@ constexpr int kBK = 64;           // K per stage (128 bytes of bf16: one swizzle
 constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;   // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;   // 32 KB
-constexpr int kEpiThreads = 128;
+constexpr int kEpiThreads = 256;
 constexpr int kProdThreads = 32;
 constexpr int kMmaWarp = (kEpiThreads + kProdThreads) / 32;
 constexpr int kGemmThreads = kEpiThreads + kProdThreads + 32;
 constexpr int kTmemCols = 2 * kBN;
-constexpr int kStagePitch = 36;  // floats per staged row (16-byte aligned, few bank conflicts)
-constexpr size_t kEpiStageBytes = 4 * 32 * kStagePitch * 4;
+// Staging tile of one epilogue warp: 32 rows x 32 floats, the 16-byte slot q of
+// row r stored at slot q ^ (r & 7) (conflict-free row-wise writes and 8-lane
+// row reads without padding).
+constexpr size_t kEpiStageBytes = (kEpiThreads / 32) * 32 * 32 * 4;
 constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 256 + kEpiStageBytes;
 
 struct GemmArgs {
@@ -49,18 +60,22 @@ struct GemmArgs {
   const int32_t* expert_ids;      // [cap / 128]
   const int32_t* ntpp;            // [1] padded rows in use
   const float* topk_w;            // [num_pairs] route weights
+  const float* sa;                // FP8: per-row scales of the A operand [cap]
+  const float* sw;                // FP8: per-channel weight scales [E, H]
   float* y_acc;                   // [T, H] fp32 accumulator
   int* err;
   int num_pairs, topk;
-  int K;                          // reduction length (I)
+  int K;                          // reduction length (I), in elements
   int H;
   int n_tiles;                    // n-blocks per m-block
   int b_rows_per_expert;          // rows of the 2D weight view per expert (H)
 };
 
+template <bool F8>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_down_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const GemmArgs args) {
+  constexpr int kElemsPerStep = F8 ? 2 * kBK : kBK;  // K elements per 128-byte step
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -111,7 +126,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int m_tiles = __ldg(args.ntpp) / kBM;
   const int tiles = m_tiles * args.n_tiles;
-  const int kblocks = args.K / kBK;
+  const int kblocks = args.K / kElemsPerStep;
 
   if (warp == kEpiThreads / 32) {
     // ------------------------------------------------------------ TMA producer
@@ -130,9 +145,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t a_dst = sA + stage * kABytes;
           const uint32_t b_dst = sB + stage * kBBytes;
           ptx::mbar_arrive_expect_tx(full_bar(stage), kBBytes + kABytes);
-          ptx::tma_load_2d(b_dst, &map_b, full_bar(stage), kb * kBK, b_row0);
-          ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(stage), kb * kBK, b_row0 + kBM);
-          ptx::tma_load_2d(a_dst, &map_a, full_bar(stage), kb * kBK, mt * kBM);
+          ptx::tma_load_2d(b_dst, &map_b, full_bar(stage), kb * kElemsPerStep, b_row0);
+          ptx::tma_load_2d(b_dst + kBBytes / 2, &map_b, full_bar(stage), kb * kElemsPerStep, b_row0 + kBM);
+          ptx::tma_load_2d(a_dst, &map_a, full_bar(stage), kb * kElemsPerStep, mt * kBM);
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -147,7 +162,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (ptx::elect_one()) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, kBN);
+      constexpr uint32_t idesc = F8 ? ptx::idesc_e4m3_f32(kBM, kBN) : ptx::idesc_bf16_f32(kBM, kBN);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -164,8 +179,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint64_t adesc = ptx::sdesc_sw128(sA + stage * kABytes);
           const uint64_t bdesc = ptx::sdesc_sw128(sB + stage * kBBytes);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            ptx::mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < 4; ++kk) {  // 32 bytes of K per MMA
+            if constexpr (F8) ptx::mma_f8(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+            else ptx::mma_f16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          }
           ptx::mma_commit(empty_bar(stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -182,9 +199,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // shared staging tile, so that the fp32 atomics of one instruction cover
     // whole 128-byte row segments of 4 rows instead of 32 scattered 16-byte
     // pieces.
-    float* stg = reinterpret_cast<float*>(ctl + 256) + warp * 32 * kStagePitch;
-    const int r = warp * 32 + lane;  // accumulator row = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    float4* stg = reinterpret_cast<float4*>(ctl + 256) + warp * 32 * 8;
+    const int quarter = warp & 3;
+    const int chalf = warp >> 2;     // accumulator columns [128 * chalf, 128 * chalf + 128)
+    const int r = quarter * 32 + lane;  // accumulator row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     int it = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
       const int b = it & 1;
@@ -193,23 +212,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int nt = t - mt * args.n_tiles;
       const int pos = mt * kBM + r;
       const int sid = __ldg(args.sorted_ids + pos);
+      const int e_of_tile = F8 ? __ldg(args.expert_ids + mt) : 0;
       if (!ptx::mbar_wait(tfull_bar(b), tphase, abort_flag)) break;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + lane_off + b * kBN;
       {
         const bool valid = sid < args.num_pairs;
-        const float w = valid ? __ldg(args.topk_w + sid) : 0.f;
+        float w = valid ? __ldg(args.topk_w + sid) : 0.f;
+        if constexpr (F8) w *= valid ? __ldg(args.sa + pos) : 0.f;  // and the row's quantisation scale
         const int tok = valid ? sid / args.topk : -1;
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int c = chalf * (kBN / 64); c < (chalf + 1) * (kBN / 64); ++c) {
           uint32_t d[32];
           ptx::tmem_ld32(tbase + c * 32, d);
           ptx::tmem_ld_wait();
-          float4* srow = reinterpret_cast<float4*>(stg + lane * kStagePitch);
+          float4 srow[8];
+          if constexpr (F8) {
+            const float4* swc = reinterpret_cast<const float4*>(
+                args.sw + static_cast<size_t>(e_of_tile) * args.H + nt * kBN + c * 32);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            srow[q] = make_float4(w * __uint_as_float(d[4 * q]), w * __uint_as_float(d[4 * q + 1]),
-                                  w * __uint_as_float(d[4 * q + 2]), w * __uint_as_float(d[4 * q + 3]));
+            for (int q = 0; q < 8; ++q) {
+              const float4 cs = __ldg(swc + q);
+              srow[q] = make_float4(w * cs.x * __uint_as_float(d[4 * q]), w * cs.y * __uint_as_float(d[4 * q + 1]),
+                                    w * cs.z * __uint_as_float(d[4 * q + 2]), w * cs.w * __uint_as_float(d[4 * q + 3]));
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              srow[q] = make_float4(w * __uint_as_float(d[4 * q]), w * __uint_as_float(d[4 * q + 1]),
+                                    w * __uint_as_float(d[4 * q + 2]), w * __uint_as_float(d[4 * q + 3]));
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) stg[lane * 8 + (q ^ (lane & 7))] = srow[q];
           __syncwarp();
           // 8 lanes add one row's 32 floats (128 contiguous bytes) into its token row
 #pragma unroll
@@ -217,7 +251,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int rl = i * 4 + (lane >> 3);
             const int q = lane & 7;
             const int trow = __shfl_sync(0xffffffffu, tok, rl);
-            const float4 v = reinterpret_cast<const float4*>(stg + rl * kStagePitch)[q];
+            const float4 v = stg[rl * 8 + (q ^ (rl & 7))];
             if (trow >= 0)
               atomicAdd(reinterpret_cast<float4*>(args.y_acc + static_cast<size_t>(trow) * args.H + nt * kBN +
                                                   c * 32) + q, v);
@@ -298,6 +332,20 @@ bool make_tmap_bf16_2d_k32(CUtensorMap* map, const void* base, uint64_t rows, ui
   return r == CUDA_SUCCESS;
 }
 
+// 2D 8-bit tensor map, box = 64 columns (bytes) x 128 rows, 64B swizzle.
+bool make_tmap_u8_2d_k64(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+  auto encode = get_encode_fn();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2D 8-bit tensor map over a row-major [rows, cols] byte matrix, box = 128 x 128,
 // 128B swizzle (tcgen05 operand) or none (staging read back by threads).
 bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, bool swizzle128) {
@@ -314,6 +362,18 @@ bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
   return r == CUDA_SUCCESS;
 }
 
+namespace {
+
+template <bool F8>
+moe_status_t launch_down(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& a, cudaStream_t s) {
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_down_kernel<F8>), static_cast<int>(kGemmSmem)))
+    return MOE_ERR_CUDA;
+  moe_down_kernel<F8><<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_a, map_b, a);
+  return launch_status();
+}
+
+}  // namespace
+
 moe_status_t launch_gemm_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, const int32_t* sorted_ids,
                               const int32_t* expert_ids, const int32_t* ntpp, const float* topk_w, float* y_acc,
                               int* err, int num_pairs, int topk, int cap, int H, int I, int E, cudaStream_t s) {
@@ -324,10 +384,23 @@ moe_status_t launch_gemm_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, c
   a.sorted_ids = sorted_ids; a.expert_ids = expert_ids; a.ntpp = ntpp; a.topk_w = topk_w; a.y_acc = y_acc;
   a.err = err; a.num_pairs = num_pairs; a.topk = topk; a.K = I; a.H = H;
   a.n_tiles = H / kBN; a.b_rows_per_expert = H;
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_down_kernel), static_cast<int>(kGemmSmem)))
-    return MOE_ERR_CUDA;
-  moe_down_kernel<<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_a, map_b, a);
-  return launch_status();
+  return launch_down<false>(map_a, map_b, a, s);
+}
+
+moe_status_t launch_gemm_down_fp8(const uint8_t* qh, const float* sh, const uint8_t* w2, const float* sw2,
+                                  const int32_t* sorted_ids, const int32_t* expert_ids, const int32_t* ntpp,
+                                  const float* topk_w, float* y_acc, int* err, int num_pairs, int topk, int cap,
+                                  int H, int I, int E, cudaStream_t s) {
+  if (I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  CUtensorMap map_a, map_b;
+  if (!make_tmap_u8_2d(&map_a, qh, static_cast<uint64_t>(cap), I, true)) return MOE_ERR_CUDA;
+  if (!make_tmap_u8_2d(&map_b, w2, static_cast<uint64_t>(E) * H, I, true)) return MOE_ERR_CUDA;
+  GemmArgs a{};
+  a.sorted_ids = sorted_ids; a.expert_ids = expert_ids; a.ntpp = ntpp; a.topk_w = topk_w; a.y_acc = y_acc;
+  a.sa = sh; a.sw = sw2;
+  a.err = err; a.num_pairs = num_pairs; a.topk = topk; a.K = I; a.H = H;
+  a.n_tiles = H / kBN; a.b_rows_per_expert = H;
+  return launch_down<true>(map_a, map_b, a, s);
 }
 
 }  // namespace moe

@@ -40,10 +40,11 @@ __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, flo
 
 template <typename T, bool E4M3>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const T* __restrict__ x, int M, int K,
-                                                         uint8_t* __restrict__ q, float* __restrict__ scales) {
+                                                         uint8_t* __restrict__ q, float* __restrict__ scales,
+                                                         const int* __restrict__ rows_dev) {
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (row >= M) return;
+  if (row >= M || (rows_dev && row >= __ldg(rows_dev))) return;
   const T* xr = x + static_cast<size_t>(row) * K;
   float amax = 0.f;
   for (int c = lane * 8; c < K; c += 256) {
@@ -79,18 +80,29 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const T* __restrict__ x
 }
 
 template <typename T>
-void launch_quant(const void* x, int M, int K, bool e4m3, void* q, float* s, cudaStream_t st) {
+void launch_quant(const void* x, int M, int K, bool e4m3, void* q, float* s, cudaStream_t st,
+                  const int* rows_dev = nullptr) {
   const int threads = 256;
   const int blocks = cdiv(M, threads / 32);
   if (e4m3)
     quant_rows_kernel<T, true><<<blocks, threads, 0, st>>>(static_cast<const T*>(x), M, K,
-                                                            static_cast<uint8_t*>(q), s);
+                                                            static_cast<uint8_t*>(q), s, rows_dev);
   else
     quant_rows_kernel<T, false><<<blocks, threads, 0, st>>>(static_cast<const T*>(x), M, K,
-                                                             static_cast<uint8_t*>(q), s);
+                                                             static_cast<uint8_t*>(q), s, rows_dev);
 }
 
 }  // namespace
+
+// Per-row e4m3 quantisation of a bf16 matrix for the fused FP8 forward: rows at
+// or past *rows_dev (read on the device) are left untouched.
+moe_status_t launch_quant_rows_e4m3_bf16(const __nv_bfloat16* x, int M, int K, uint8_t* q, float* s,
+                                         const int* rows_dev, cudaStream_t st) {
+  if (M == 0) return MOE_OK;
+  launch_quant<__nv_bfloat16>(x, M, K, true, q, s, st, rows_dev);
+  return launch_status();
+}
+
 }  // namespace moe
 
 extern "C" moe_status_t moe_quant_per_token(const void* x, int x_dt, int M, int K, int q_dt, void* q,

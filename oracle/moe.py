@@ -148,24 +148,31 @@ def fused_forward_fp8(x, gating_output, qw1, sw1, qw2, sw2, topk: int, renormali
     ``qw1`` uint8 e4m3 codes [E, 2I, H] with ``sw1`` [E, 2I]; ``qw2`` [E, H, I] with
     ``sw2`` [E, H]. Returns (y float64 [T, H], topk_weights float32, topk_ids int32).
     """
-    from . import quant
     tw, ids = routing.grouped_topk(gating_output, topk, renormalize, num_expert_group,
                                    topk_group, scoring_func, routed_scaling_factor)
     x = np.asarray(x, dtype=np.float32)
-    qx, sx = quant.quant_rows_e4m3(x)
-    dx = quant.dequant(qx, "e4m3") * sx.astype(np.float64)[:, None]        # sx[t] * deq(qx[t])
-    w1 = quant.dequant(qw1, "e4m3") * np.asarray(sw1, dtype=np.float64)[:, :, None]
-    w2 = quant.dequant(qw2, "e4m3") * np.asarray(sw2, dtype=np.float64)[:, :, None]
-    I = w1.shape[1] // 2
     T, k = ids.shape
-    y = np.zeros((T, w2.shape[1]))
+    y = np.zeros((T, np.asarray(qw2).shape[1]))
     for t in range(T):
-        for j in range(k):
-            e = ids[t, j]
-            g = w1[e, :I] @ dx[t]
-            u = w1[e, I:] @ dx[t]
-            h = _bf16_round(silu(g) * u)
-            qh, sh = quant.quant_rows_e4m3(h[None, :])
-            dh = quant.dequant(qh[0], "e4m3") * float(sh[0])
-            y[t] += float(tw[t, j]) * (w2[e] @ dh)
+        es = ids[t]
+        y[t] = token_outputs_fp8(x[t], [qw1[e] for e in es], [sw1[e] for e in es], [qw2[e] for e in es],
+                                 [sw2[e] for e in es], tw[t])
     return y, tw, ids
+
+
+def token_outputs_fp8(x_row, qw1_experts, sw1_experts, qw2_experts, sw2_experts, weights) -> np.ndarray:
+    """One token's output of the FP8 layer (steps 2-5 of ``fused_forward_fp8``) from its own
+    experts: ``qw1_experts`` list of e4m3 codes [2I, H] with ``sw1_experts`` [2I], ``qw2_experts``
+    list of [H, I] with ``sw2_experts`` [H], ``weights`` [topk] route weights."""
+    from . import quant
+    qx, sx = quant.quant_rows_e4m3(np.asarray(x_row, dtype=np.float32)[None, :])
+    dx = quant.dequant(qx[0], "e4m3") * float(sx[0])                        # sx[t] * deq(qx[t])
+    out = 0.0
+    for q1, s1, q2, s2, wj in zip(qw1_experts, sw1_experts, qw2_experts, sw2_experts, weights):
+        w1 = quant.dequant(q1, "e4m3") * np.asarray(s1, dtype=np.float64)[:, None]
+        w2 = quant.dequant(q2, "e4m3") * np.asarray(s2, dtype=np.float64)[:, None]
+        I = w1.shape[0] // 2
+        h = _bf16_round(silu(w1[:I] @ dx) * (w1[I:] @ dx))
+        qh, sh = quant.quant_rows_e4m3(h[None, :])
+        out = out + float(wj) * (w2 @ (quant.dequant(qh[0], "e4m3") * float(sh[0])))
+    return out
