@@ -11,14 +11,15 @@
 // sorted order), so both operands arrive by TMA.
 //
 // Kernel shape (one persistent CTA per SM, 320 threads):
-//   warps 0-7  epilogue: TMEM -> registers -> shared staging -> fp32 atomics
-//              (TMEM lane quarter = warp % 4, column half = warp / 4: two warps
-//              drain each accumulator row, so that the combine of a tile stays
-//              shorter than the main loop of the next when K is short, as with
-//              FP8 operands)
-//   warp 8     one thread sends A and B of every K step by TMA through the
+//   warps 0-(P-1)  epilogue: TMEM -> registers -> shared staging -> fp32 atomics
+//              (TMEM lane quarter = warp % 4). The bf16 instance has P = 4 warps;
+//              the FP8 instance P = 8 (column half = warp / 4: two warps drain
+//              each accumulator row), so that the combine of a tile stays shorter
+//              than the main loop of the next, which FP8 operands halve. (Eight
+//              warps made the bf16 instance 4 % slower.)
+//   warp P     one thread sends A and B of every K step by TMA through the
 //              4-slot ring
-//   warp 9     TMEM allocation and the single MMA-issuing thread
+//   warp P+1   TMEM allocation and the single MMA-issuing thread
 // The kernel is written in bytes of K: a K step is one 128-byte swizzle row of
 // both operands (64 bf16 or 128 FP8-e4m3 values), four MMAs of 32 bytes of K.
 // The FP8 instance (the low-precision GMM article's layer: per-token
@@ -44,15 +45,14 @@ constexpr int kBK = 64;           // K per stage (128 bytes of bf16: one swizzle
 constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;   // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;   // 32 KB
-constexpr int kEpiThreads = 256;
+template <bool F8> constexpr int epi_threads() { return F8 ? 256 : 128; }
 constexpr int kProdThreads = 32;
-constexpr int kMmaWarp = (kEpiThreads + kProdThreads) / 32;
-constexpr int kGemmThreads = kEpiThreads + kProdThreads + 32;
+template <bool F8> constexpr int gemm_threads() { return epi_threads<F8>() + kProdThreads + 32; }
 constexpr int kTmemCols = 2 * kBN;
 // Staging tile of one epilogue warp: 32 rows x 32 floats, the 16-byte slot q of
 // row r stored at slot q ^ (r & 7) (conflict-free row-wise writes and 8-lane
 // row reads without padding).
-constexpr size_t kEpiStageBytes = (kEpiThreads / 32) * 32 * 32 * 4;
+constexpr size_t kEpiStageBytes = (epi_threads<true>() / 32) * 32 * 32 * 4;  // sized for the larger instance
 constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 256 + kEpiStageBytes;
 
 struct GemmArgs {
@@ -72,10 +72,12 @@ struct GemmArgs {
 };
 
 template <bool F8>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<F8>(), 1)
     moe_down_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const GemmArgs args) {
   constexpr int kElemsPerStep = F8 ? 2 * kBK : kBK;  // K elements per 128-byte step
+  constexpr int kEpiThreads = epi_threads<F8>();
+  constexpr int kMmaWarp = (kEpiThreads + kProdThreads) / 32;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -200,8 +202,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // whole 128-byte row segments of 4 rows instead of 32 scattered 16-byte
     // pieces.
     float4* stg = reinterpret_cast<float4*>(ctl + 256) + warp * 32 * 8;
+    constexpr int kParts = kEpiThreads / 128;  // warps per TMEM lane quarter
     const int quarter = warp & 3;
-    const int chalf = warp >> 2;     // accumulator columns [128 * chalf, 128 * chalf + 128)
+    const int chalf = warp >> 2;     // accumulator columns [kBN / kParts * chalf, ...) of this warp
     const int r = quarter * 32 + lane;  // accumulator row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     int it = 0;
@@ -222,7 +225,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if constexpr (F8) w *= valid ? __ldg(args.sa + pos) : 0.f;  // and the row's quantisation scale
         const int tok = valid ? sid / args.topk : -1;
 #pragma unroll 1
-        for (int c = chalf * (kBN / 64); c < (chalf + 1) * (kBN / 64); ++c) {
+        for (int c = chalf * (kBN / 32 / kParts); c < (chalf + 1) * (kBN / 32 / kParts); ++c) {
           uint32_t d[32];
           ptx::tmem_ld32(tbase + c * 32, d);
           ptx::tmem_ld_wait();
@@ -368,7 +371,7 @@ template <bool F8>
 moe_status_t launch_down(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& a, cudaStream_t s) {
   if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_down_kernel<F8>), static_cast<int>(kGemmSmem)))
     return MOE_ERR_CUDA;
-  moe_down_kernel<F8><<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_a, map_b, a);
+  moe_down_kernel<F8><<<num_sms(), gemm_threads<F8>(), kGemmSmem, s>>>(map_a, map_b, a);
   return launch_status();
 }
 

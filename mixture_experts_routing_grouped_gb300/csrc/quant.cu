@@ -8,8 +8,10 @@
 // codes are exactly those of the same arithmetic done on the host. An all-zero
 // row gets scale 1 and codes 0.
 //
-// One warp per row; the row is read twice (absmax, then quantise), the second
-// time mostly from L1/L2.
+// Rows of up to 2048 bf16 (1024 fp32) values are loaded once into the registers
+// of 8, 16 or 32 lanes (several rows per warp), and the absmax and the codes are
+// computed from there; longer rows take one warp each and are read twice
+// (absmax, then quantise), the second time mostly from L1/L2.
 #include "common.cuh"
 
 #include <cuda_fp8.h>
@@ -36,6 +38,15 @@ __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, flo
     v[2 * i] = __uint_as_float(w[i] << 16);
     v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
+}
+
+// Code of x / s (an IEEE fp32 quotient) for one value.
+template <bool E4M3>
+__device__ __forceinline__ uint32_t quant_code(float v, float s) {
+  const float r = __fdiv_rn(v, s);
+  if (E4M3) return static_cast<uint32_t>(__nv_cvt_float_to_fp8(r, __NV_SATFINITE, __NV_E4M3));
+  const float rq = fminf(fmaxf(rintf(r), -127.f), 127.f);
+  return static_cast<uint32_t>(static_cast<int>(rq)) & 0xffu;
 }
 
 template <typename T, bool E4M3>
@@ -65,31 +76,121 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const T* __restrict__ x
     uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float r = __fdiv_rn(v[i], s);
-      uint32_t code;
-      if (E4M3) {
-        code = static_cast<uint32_t>(__nv_cvt_float_to_fp8(r, __NV_SATFINITE, __NV_E4M3));
-      } else {
-        const float rq = fminf(fmaxf(rintf(r), -127.f), 127.f);
-        code = static_cast<uint32_t>(static_cast<int>(rq)) & 0xffu;
-      }
+      const uint32_t code = quant_code<E4M3>(v[i], s);
       if (i < 4) lo |= code << (8 * i); else hi |= code << (8 * (i - 4));
     }
     *reinterpret_cast<uint2*>(qr + c) = make_uint2(lo, hi);
   }
 }
 
+// Raw 16-byte chunks of 8 values: bf16 rows keep one uint4 per chunk, fp32 rows two.
+template <typename T> struct Chunk;
+template <> struct Chunk<__nv_bfloat16> {
+  uint4 u;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { u = __ldg(reinterpret_cast<const uint4*>(p)); }
+  __device__ __forceinline__ void values(float (&v)[8]) const {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+template <> struct Chunk<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = __ldg(reinterpret_cast<const float4*>(p));
+    b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  }
+  __device__ __forceinline__ void values(float (&v)[8]) const {
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+};
+
+// Register-resident variant: L lanes per row (32 / L rows per warp), lane s of a
+// row holding its chunks s + L i (i < C) in registers, K <= 8 L C. All of a
+// lane's loads are in flight together and the row is read once; a row's chain
+// (loads, absmax, L-lane reduction, scale, codes) is short enough, and there are
+// enough rows per warp, that the kernel streams instead of waiting on one
+// row's latency per warp.
+template <typename T, bool E4M3, int L, int C>
+__global__ void __launch_bounds__(256) quant_rows_reg_kernel(const T* __restrict__ x, int M, int K,
+                                                             uint8_t* __restrict__ q, float* __restrict__ scales,
+                                                             const int* __restrict__ rows_dev) {
+  const int gl = blockIdx.x * blockDim.x + threadIdx.x;
+  const int row = gl / L;
+  const int sub = gl & (L - 1);
+  const int m = rows_dev ? min(M, __ldg(rows_dev)) : M;
+  const bool live = row < m;
+  const T* xr = x + static_cast<size_t>(live ? row : 0) * K;
+  Chunk<T> raw[C];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    const int c = (sub + L * i) * 8;
+    if (live && c < K) raw[i].load(xr + c);
+  }
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    const int c = (sub + L * i) * 8;
+    if (live && c < K) {
+      float v[8];
+      raw[i].values(v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (!live) return;
+  const float qmax = E4M3 ? 448.0f : 127.0f;
+  const float sc = (amax == 0.f) ? 1.0f : __fdiv_rn(amax, qmax);
+  if (sub == 0) scales[row] = sc;
+  uint8_t* qr = q + static_cast<size_t>(row) * K;
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    const int c = (sub + L * i) * 8;
+    if (c < K) {
+      float v[8];
+      raw[i].values(v);
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        lo |= quant_code<E4M3>(v[j], sc) << (8 * j);
+        hi |= quant_code<E4M3>(v[j + 4], sc) << (8 * j);
+      }
+      *reinterpret_cast<uint2*>(qr + c) = make_uint2(lo, hi);
+    }
+  }
+}
+
+template <typename T, bool E4M3, int L, int C>
+void launch_reg(const T* x, int M, int K, uint8_t* q, float* s, cudaStream_t st, const int* rows_dev) {
+  const int rows_per_block = 256 / L;
+  quant_rows_reg_kernel<T, E4M3, L, C><<<cdiv(M, rows_per_block), 256, 0, st>>>(x, M, K, q, s, rows_dev);
+}
+
+// Lanes per row: the fewest (>= 8) that keep a lane's chunks within C (8 for bf16
+// rows, 4 for fp32 rows: 32 registers of raw data, so that enough warps stay
+// resident to hide each row's dependent chain); rows longer than 32 lanes' worth
+// take the two-pass kernel.
+template <typename T, bool E4M3>
+void launch_quant_t(const T* x, int M, int K, uint8_t* q, float* s, cudaStream_t st, const int* rows_dev) {
+  constexpr int C = sizeof(T) == 2 ? 8 : 4;
+  if (K <= 8 * 8 * C) launch_reg<T, E4M3, 8, C>(x, M, K, q, s, st, rows_dev);
+  else if (K <= 8 * 16 * C) launch_reg<T, E4M3, 16, C>(x, M, K, q, s, st, rows_dev);
+  else if (K <= 8 * 32 * C) launch_reg<T, E4M3, 32, C>(x, M, K, q, s, st, rows_dev);
+  else quant_rows_kernel<T, E4M3><<<cdiv(M, 8), 256, 0, st>>>(x, M, K, q, s, rows_dev);
+}
+
 template <typename T>
 void launch_quant(const void* x, int M, int K, bool e4m3, void* q, float* s, cudaStream_t st,
                   const int* rows_dev = nullptr) {
-  const int threads = 256;
-  const int blocks = cdiv(M, threads / 32);
   if (e4m3)
-    quant_rows_kernel<T, true><<<blocks, threads, 0, st>>>(static_cast<const T*>(x), M, K,
-                                                            static_cast<uint8_t*>(q), s, rows_dev);
+    launch_quant_t<T, true>(static_cast<const T*>(x), M, K, static_cast<uint8_t*>(q), s, st, rows_dev);
   else
-    quant_rows_kernel<T, false><<<blocks, threads, 0, st>>>(static_cast<const T*>(x), M, K,
-                                                             static_cast<uint8_t*>(q), s, rows_dev);
+    launch_quant_t<T, false>(static_cast<const T*>(x), M, K, static_cast<uint8_t*>(q), s, st, rows_dev);
 }
 
 }  // namespace
