@@ -487,10 +487,16 @@ def bench_cublas_context(torch, dev, flush, cfg, ids, args):
 
 
 def bench_lowp(moe, synth, torch, dev, flush, peaks, args):
-    """Low-precision grouped GEMM, M=2048, K=N=4096, E=32 Zipf groups, bf16 out, INT8 and FP8-e4m3."""
-    cfg = synth.lowp_config()
+    """Low-precision grouped GEMM, M=2048, K=N=4096, E=32 Zipf groups, bf16 out, INT8 and FP8-e4m3;
+    and the small-K case K=768, N=3072 under "small_k"."""
+    out = bench_lowp_cfg(moe, synth, torch, dev, flush, peaks, args, synth.lowp_config())
+    out["small_k"] = bench_lowp_cfg(moe, synth, torch, dev, flush, peaks, args, synth.lowp_small_k_config())
+    return out
+
+
+def bench_lowp_cfg(moe, synth, torch, dev, flush, peaks, args, cfg):
     d = synth.gmm_inputs(cfg, dev)
-    out = {}
+    out = {"workload": cfg.name}
     sizes = d["expert_sizes"].cpu().tolist()
     n_active = sum(1 for s_ in sizes if s_ > 0)
     flops = 2.0 * cfg.M * cfg.N * cfg.K

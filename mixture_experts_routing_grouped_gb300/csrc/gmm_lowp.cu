@@ -261,17 +261,31 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
-      for (int it = 0;; ++it) {
+      // The next task is claimed (an L2 round trip) and published three K steps
+      // before the current task's last load, so that its loads follow the current
+      // ones without a gap: with small K a task is only a few K steps, and a
+      // claim at the task boundary left the ring empty for a claim's latency every
+      // task (the article's small-K case, section 4.2, interleaves two experts per
+      // block for the same reason).
+      auto publish = [&](int it, int t) -> bool {
         const int q = it % kQ;
-        if (!ptx::mbar_wait(qempty_bar(q), (static_cast<uint32_t>(it / kQ) & 1u) ^ 1u, abort_flag)) break;
-        const int t = atomicAdd(args.counter, 1);
+        if (!ptx::mbar_wait(qempty_bar(q), (static_cast<uint32_t>(it / kQ) & 1u) ^ 1u, abort_flag)) return false;
         tq[q] = t;
         ptx::mbar_arrive(qfull_bar(q));
-        if (t >= num_tasks) break;
+        return true;
+      };
+      const int claim_at = kblocks > 3 ? kblocks - 3 : 0;
+      int t = atomicAdd(args.counter, 1);
+      bool ok = publish(0, t);
+      for (int it = 0; ok && t < num_tasks; ++it) {
         const Task k = decode_task(args, n_tiles, t);
         const int wrow = k.e * args.N + k.nt * kLBN;
-        bool ok = true;
+        int t_next = num_tasks;
         for (int kb = 0; kb < kblocks; ++kb) {
+          if (kb == claim_at) {
+            t_next = atomicAdd(args.counter, 1);
+            if (!publish(it + 1, t_next)) { ok = false; break; }
+          }
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           if constexpr (I8) {
             const uint32_t dst = sbase + stage * kTile8;  // weight codes
@@ -286,7 +300,7 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
+        t = t_next;
       }
 #pragma unroll
       for (int s = 0; s < kStages; ++s) {

@@ -232,6 +232,11 @@ def lowp_config() -> GmmConfig:
     return GmmConfig("gmm_lowp_M2048_K4096_N4096_E32_zipf1.2", M=2048, K=4096, N=4096, E=32)
 
 
+def lowp_small_k_config() -> GmmConfig:
+    """The low-precision GMM article's small-K case (section 4.2: K=768, N=3072), 32 Zipf groups."""
+    return GmmConfig("gmm_lowp_M2048_K768_N3072_E32_zipf1.2", M=2048, K=768, N=3072, E=32)
+
+
 def _perm(n: int, seed: int, tag: int) -> list[int]:
     """Fisher-Yates permutation of range(n) driven by the counter generator."""
     u = uniform_u32(stream_key(seed, tag), 0, n, "cpu").tolist()

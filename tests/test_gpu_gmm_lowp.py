@@ -108,9 +108,9 @@ def test_gmm_inconsistent_metadata_is_reported_and_skipped():
     assert np.array_equal(o[:32], ref.astype(np.float32))
 
 
-@pytest.fixture(scope="module")
-def lowp_workload():
-    cfg = synth.lowp_config()
+@pytest.fixture(scope="module", params=[synth.lowp_config(), synth.lowp_small_k_config()], ids=lambda c: c.name)
+def lowp_workload(request):
+    cfg = request.param
     d = synth.gmm_inputs(cfg, "cuda")
     x = d["x"].cpu().numpy()
     w = d["w"].cpu().numpy().reshape(cfg.E * cfg.N, cfg.K)

@@ -98,3 +98,23 @@ def test_gmm_lowp_workspace_holds_the_widened_activations(L):
     for M, K, N, E in ((2048, 4096, 4096, 32), (1, 128, 128, 1), (0, 256, 128, 4)):
         assert L.gmm_lowp_workspace_size(M, K, N, E) >= M * K * 2 + 256
     assert L.gmm_lowp_workspace_size(16, 128, 128, 0) == 0
+
+
+def test_fused_fp8_validation_and_sizes(L):
+    f = L.moe_fused_forward_fp8
+    ws = L.moe_fused_forward_fp8_workspace_size(4096, 2048, 768, 128, 8)
+    cap = oalign.max_padded(4096 * 8, 128, 128)
+    # the bf16 layout, plus e4m3 codes of x and of h with their scales
+    assert ws >= cap * 768 * 2 + 4096 * 2048 * 4 + 4096 * 2048 + cap * 768
+    assert L.moe_fused_forward_fp8_workspace_size(16, 512, 256, 0, 2) == 0
+    args = lambda H, I, wsb, wsp=FAKE, s1=FAKE, s2=FAKE: (FAKE, FAKE, FAKE, s1, FAKE, s2, 64, H, I, 8, 1, 1, 2, 0, 1,
+                                                         1.0, FAKE, FAKE, FAKE, wsp, wsb, None)
+    assert f(*args(100, 256, 1 << 30)) == 2          # H not a multiple of 256
+    assert f(*args(512, 200, 1 << 30)) == 2          # I not a multiple of 128
+    assert f(*args(512, 256, 1 << 30, s1=None)) == 1  # missing gate_up scales
+    assert f(*args(512, 256, 1 << 30, s2=None)) == 1  # missing down scales
+    assert f(*args(512, 256, 1 << 30, s1=ctypes.c_void_p(0x10004))) == 2  # scales not 16-byte aligned
+    need = L.moe_fused_forward_fp8_workspace_size(64, 512, 256, 8, 2)
+    assert need > L.moe_fused_forward_workspace_size(64, 512, 256, 8, 2)
+    assert f(*args(512, 256, need - 1)) == 3
+    assert f(*args(512, 256, need, ctypes.c_void_p(0x10010))) == 3  # workspace not 256-byte aligned
