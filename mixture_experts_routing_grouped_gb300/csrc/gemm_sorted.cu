@@ -214,53 +214,59 @@ __global__ void __launch_bounds__(gemm_threads<F8>(), 1)
       const int mt = t / args.n_tiles;
       const int nt = t - mt * args.n_tiles;
       const int pos = mt * kBM + r;
+      // the row's pair, token and weights are loaded before waiting for the accumulator
       const int sid = __ldg(args.sorted_ids + pos);
+      const bool valid = sid < args.num_pairs;
+      float w = valid ? __ldg(args.topk_w + sid) : 0.f;
+      if constexpr (F8) w *= valid ? __ldg(args.sa + pos) : 0.f;  // and the row's quantisation scale
+      const int tok = valid ? sid / args.topk : -1;
       const int e_of_tile = F8 ? __ldg(args.expert_ids + mt) : 0;
       if (!ptx::mbar_wait(tfull_bar(b), tphase, abort_flag)) break;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + lane_off + b * kBN;
-      {
-        const bool valid = sid < args.num_pairs;
-        float w = valid ? __ldg(args.topk_w + sid) : 0.f;
-        if constexpr (F8) w *= valid ? __ldg(args.sa + pos) : 0.f;  // and the row's quantisation scale
-        const int tok = valid ? sid / args.topk : -1;
-#pragma unroll 1
-        for (int c = chalf * (kBN / 32 / kParts); c < (chalf + 1) * (kBN / 32 / kParts); ++c) {
-          uint32_t d[32];
-          ptx::tmem_ld32(tbase + c * 32, d);
-          ptx::tmem_ld_wait();
-          float4 srow[8];
-          if constexpr (F8) {
-            const float4* swc = reinterpret_cast<const float4*>(
-                args.sw + static_cast<size_t>(e_of_tile) * args.H + nt * kBN + c * 32);
+      // The TMEM load of the next 32 columns is issued as soon as the current
+      // one has landed, so that it overlaps this chunk's scaling, staging and
+      // atomics (FP8 tiles have half the main loop to hide the combine behind).
+      constexpr int kCh = kBN / 32 / kParts;  // 32-column chunks per warp
+      const int c0 = chalf * kCh;
+      uint32_t d[2][32];
+      ptx::tmem_ld32(tbase + c0 * 32, d[0]);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 cs = __ldg(swc + q);
-              srow[q] = make_float4(w * cs.x * __uint_as_float(d[4 * q]), w * cs.y * __uint_as_float(d[4 * q + 1]),
-                                    w * cs.z * __uint_as_float(d[4 * q + 2]), w * cs.w * __uint_as_float(d[4 * q + 3]));
-            }
-          } else {
+      for (int ci = 0; ci < kCh; ++ci) {
+        const int c = c0 + ci;
+        float4 cs[8];
+        if constexpr (F8) {
+          const float4* swc =
+              reinterpret_cast<const float4*>(args.sw + static_cast<size_t>(e_of_tile) * args.H + nt * kBN + c * 32);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              srow[q] = make_float4(w * __uint_as_float(d[4 * q]), w * __uint_as_float(d[4 * q + 1]),
-                                    w * __uint_as_float(d[4 * q + 2]), w * __uint_as_float(d[4 * q + 3]));
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) stg[lane * 8 + (q ^ (lane & 7))] = srow[q];
-          __syncwarp();
-          // 8 lanes add one row's 32 floats (128 contiguous bytes) into its token row
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rl = i * 4 + (lane >> 3);
-            const int q = lane & 7;
-            const int trow = __shfl_sync(0xffffffffu, tok, rl);
-            const float4 v = stg[rl * 8 + (q ^ (rl & 7))];
-            if (trow >= 0)
-              atomicAdd(reinterpret_cast<float4*>(args.y_acc + static_cast<size_t>(trow) * args.H + nt * kBN +
-                                                  c * 32) + q, v);
-          }
-          __syncwarp();
+          for (int q = 0; q < 8; ++q) cs[q] = __ldg(swc + q);
         }
+        ptx::tmem_ld_wait();
+        if (ci + 1 < kCh) ptx::tmem_ld32(tbase + (c + 1) * 32, d[(ci + 1) & 1]);
+        const uint32_t* dc = d[ci & 1];
+        float4 srow[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 k = F8 ? make_float4(w * cs[q].x, w * cs[q].y, w * cs[q].z, w * cs[q].w)
+                              : make_float4(w, w, w, w);
+          srow[q] = make_float4(k.x * __uint_as_float(dc[4 * q]), k.y * __uint_as_float(dc[4 * q + 1]),
+                                k.z * __uint_as_float(dc[4 * q + 2]), k.w * __uint_as_float(dc[4 * q + 3]));
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) stg[lane * 8 + (q ^ (lane & 7))] = srow[q];
+        __syncwarp();
+        // 8 lanes add one row's 32 floats (128 contiguous bytes) into its token row
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rl = i * 4 + (lane >> 3);
+          const int q = lane & 7;
+          const int trow = __shfl_sync(0xffffffffu, tok, rl);
+          const float4 v = stg[rl * 8 + (q ^ (rl & 7))];
+          if (trow >= 0)
+            atomicAdd(reinterpret_cast<float4*>(args.y_acc + static_cast<size_t>(trow) * args.H + nt * kBN +
+                                                c * 32) + q, v);
+        }
+        __syncwarp();
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty_bar(b));
