@@ -586,7 +586,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-extra", action="store_true", help="skip the decode and routing sub-benchmarks")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["routing", "decode", "lowp"],
+    ap.add_argument("--only", choices=["routing", "decode", "lowp", "fp8"],
                     help="run just one sub-benchmark on one GPU and print its JSON (profiling cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -607,8 +607,14 @@ def main():
         peaks, _ = load_peaks()
         dev = torch.device("cuda", local_rank)
         flush = L2Flush(torch, dev)
-        fn = {"routing": bench_routing, "decode": bench_decode, "lowp": bench_lowp}[args.only]
-        print(json.dumps({args.only: fn(moe, synth, torch, dev, flush, peaks, args)}), flush=True)
+        if args.only == "fp8":
+            cfg = synth.prefill_config()
+            res = bench_fp8_layer(moe, torch, dev, flush, peaks, args, cfg, synth.moe_activations(cfg, dev),
+                                  synth.moe_weights(cfg, dev))
+        else:
+            fn = {"routing": bench_routing, "decode": bench_decode, "lowp": bench_lowp}[args.only]
+            res = fn(moe, synth, torch, dev, flush, peaks, args)
+        print(json.dumps({args.only: res}), flush=True)
         return
 
     if world > 1:
