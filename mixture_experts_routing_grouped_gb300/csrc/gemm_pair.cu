@@ -80,7 +80,9 @@ constexpr int kTmemCols = 2 * kBN;
 constexpr int kQ = 4;                                        // claimed-tile queue entries
 constexpr int kQConsumers = kStages + 1 + kEpiWarps;          // gather warps, MMA thread, epilogue warps
 constexpr int kStagePitch = 18;  // 32-bit words per staged row: 16 bf16 pairs, 8-byte aligned rows
-constexpr size_t kCtlBytes = 256 + 4 * (MOE_MAX_EXPERTS + 1) + 12 + kEpiWarps * 32 * kStagePitch * 4;
+constexpr int kScaleFloats = 128;  // FP8: per epilogue warp, gate and up channel scales of its two column chunks
+constexpr size_t kCtlBytes =
+    256 + 4 * (MOE_MAX_EXPERTS + 1) + 12 + kEpiWarps * 32 * kStagePitch * 4 + kEpiWarps * kScaleFloats * 4;
 constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + kCtlBytes;
 
 struct GemmArgs {
@@ -389,6 +391,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else {
     float* stg = stg_all + warp * 32 * kStagePitch;
+    float* scl = stg_all + kEpiWarps * 32 * kStagePitch + warp * kScaleFloats;  // [chunk 0..1][gate 32 | up 32]
     const int quarter = warp & 3;       // TMEM lane quarter (rows 32*quarter ..)
     const int cpart = warp >> 2;        // column chunks [2*cpart, 2*cpart + 2) of each row half
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -404,17 +407,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int t;
       if (!read_tile(it, t, true) || t >= tiles) break;
       const TileInfo ti = decode_tile(pfx, args.offsets, args.E, args.n_tiles, t);
+      const int n0 = ti.nt * kHalf;
+      // FP8: while the tile's MMAs run, fetch the token scale of this lane's row in
+      // each row half and stage the warp's 128 channel scales in shared memory, so
+      // that no global load sits between the accumulator and the SwiGLU.
+      float rs_half[2] = {1.f, 1.f};
+      if constexpr (F8) {
+        const int cl = lane >> 4, part = (lane >> 3) & 1, q = lane & 7;
+        const float* src =
+            args.sw + static_cast<size_t>(ti.e) * 2 * args.I + part * args.I + n0 + (2 * cpart + cl) * 32 + q * 4;
+        reinterpret_cast<float4*>(scl)[lane] = __ldg(reinterpret_cast<const float4*>(src));
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          const int tok = hb < ti.nblk ? __ldg(args.sorted_tok + ti.row0 + hb * kHalf + quarter * 32 + lane) : -1;
+          rs_half[hb] = tok >= 0 ? __ldg(args.sx + tok) : 0.f;  // 0 for padding rows
+        }
+        __syncwarp();
+      }
       if (!ptx::mbar_wait(tfull_bar, static_cast<uint32_t>(it) & 1u, abort_flag)) break;
       ptx::tc_fence_after();
-      const int n0 = ti.nt * kHalf;
       for (int half = 0; half < ti.nblk; ++half) {
         const uint32_t tbase = tmem_base + lane_off + half * kBN;
         const int rowbase = ti.row0 + half * kHalf + quarter * 32;
-        float rs = 1.f;  // FP8: the row's token scale (0 for padding rows)
-        if constexpr (F8) {
-          const int tok = __ldg(args.sorted_tok + rowbase + lane);
-          rs = tok >= 0 ? __ldg(args.sx + tok) : 0.f;
-        }
+        const float rs = rs_half[half];
 #pragma unroll 1
         for (int c = 2 * cpart; c < 2 * cpart + 2; ++c) {
           uint32_t g[32], u[32];
@@ -423,12 +438,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ptx::tmem_ld_wait();
           if constexpr (F8) {
             // g = sx[token] * sw[e, n] * acc_g, u = sx[token] * sw[e, I + n] * acc_u
-            const float* swg = args.sw + static_cast<size_t>(ti.e) * 2 * args.I + n0 + c * 32;
-            const float* swu = swg + args.I;
+            const float4* swg = reinterpret_cast<const float4*>(scl + (c - 2 * cpart) * 64);
+            const float4* swu = swg + 8;
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
-              const float4 a = __ldg(reinterpret_cast<const float4*>(swg + j));
-              const float4 b = __ldg(reinterpret_cast<const float4*>(swu + j));
+              const float4 a = swg[j / 4];
+              const float4 b = swu[j / 4];
               g[j] = __float_as_uint(rs * a.x * __uint_as_float(g[j]));
               g[j + 1] = __float_as_uint(rs * a.y * __uint_as_float(g[j + 1]));
               g[j + 2] = __float_as_uint(rs * a.z * __uint_as_float(g[j + 2]));
