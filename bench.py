@@ -450,6 +450,8 @@ def bench_fp8_layer(moe, torch, dev, flush, peaks, args, cfg, acts, W):
             "gate_up_TFLOP/s": round(gu_tf, 1), "down_TFLOP/s": round(dn_tf, 1),
             "fp8_peak_TFLOP/s": peak8, "gate_up_frac_fp8_peak": round(gu_tf / peak8, 4),
             "peak_source": "2 x bf16_tflops (burst) of measured: the nominal fp8 / bf16 dense ratio",
+            "traffic_bytes_per_launch": {"gemm_gate_up": kernel_traffic("pair::moe_gate_up_kernel<1>"),
+                                         "gemm_down": kernel_traffic("moe_down_kernel<1>")},
             "gpu_launches_per_step": 8}
 
 
