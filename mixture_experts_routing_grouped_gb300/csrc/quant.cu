@@ -5,8 +5,9 @@
 // absmax(row) / 127 and q = clamp(round(x / scale), -127, 127) for INT8; the
 // FP8-e4m3 variant uses absmax / 448 and a round-to-nearest-even, saturating
 // conversion. Scale and quotient are IEEE fp32 operations (no fast-math), so the
-// codes are exactly those of the same arithmetic done on the host. An all-zero
-// row gets scale 1 and codes 0.
+// codes are exactly those of the same arithmetic done on the host; the quotient is
+// formed as x * RN(1/scale) wherever an error bound shows that gives the same code,
+// else by the correctly rounded division. An all-zero row gets scale 1 and codes 0.
 //
 // Rows of up to 2048 bf16 (1024 fp32) values are loaded once into the registers
 // of 8, 16 or 32 lanes (several rows per warp), and the absmax and the codes are
@@ -40,13 +41,71 @@ __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, flo
   }
 }
 
-// Code of x / s (an IEEE fp32 quotient) for one value.
+// Code of r, the fp32 quotient x / s, for one value.
 template <bool E4M3>
-__device__ __forceinline__ uint32_t quant_code(float v, float s) {
-  const float r = __fdiv_rn(v, s);
+__device__ __forceinline__ uint32_t code_of(float r) {
   if (E4M3) return static_cast<uint32_t>(__nv_cvt_float_to_fp8(r, __NV_SATFINITE, __NV_E4M3));
   const float rq = fminf(fmaxf(rintf(r), -127.f), 127.f);
   return static_cast<uint32_t>(static_cast<int>(rq)) & 0xffu;
+}
+
+// Whether y = x * RN(1/s) may round to another code than RN(x / s) does. With
+// u = 2^-24, RN(1/s) = (1/s)(1 + e1) and y = (x/s)(1 + e1)(1 + e2), |e1|, |e2| <= u, so
+// |y - x/s| < 2 ulp(x/s) and y, RN(x/s) are at most 2 ulps apart (one binade: the
+// boundaries below sit mid-binade). The two codes can then differ only where a
+// rounding boundary of the target lies within 2 ulps of y; the test takes 3.
+//  e4m3, |y| >= 2^-6: the boundaries are the midpoints 2^e (1 + (2m+1)/16), whose fp32
+//    encodings have bit 19 set and bits 18..0 clear; 0 < |y| < 2^-6 (e4m3 subnormals,
+//    whose boundaries are spread over several binades) always takes the exact path.
+//  INT8: the boundaries are the half-integers; |y - rint(y)| is exact, and 2^-14
+//    exceeds 3 ulps for every |y| < 128.
+template <bool E4M3>
+__device__ __forceinline__ bool needs_exact(float y) {
+  if (E4M3) {
+    const uint32_t a = __float_as_uint(y) & 0x7fffffffu;
+    return (a - 1u < 0x3c800000u - 1u) || ((a & 0xfffffu) - 0x7fffdu < 7u);
+  }
+  return fabsf(fabsf(y - rintf(y)) - 0.5f) <= 0x1p-14f;
+}
+
+// Per-row constants of the quotient: s, RN(1/s), and whether the product path is
+// valid for the row (s and 1/s normal, so that neither rounding step underflows
+// outside the e4m3 subnormal range, which is checked per value).
+struct RowScale {
+  float s, rs;
+  bool exact;
+};
+
+__device__ __forceinline__ RowScale row_scale(float sc) {
+  RowScale r;
+  r.s = sc;
+  r.rs = __frcp_rn(sc);
+  r.exact = !(sc >= 0x1p-125f && sc <= 0x1p125f);
+  return r;
+}
+
+// Codes of eight values x / s, packed little-endian: x * RN(1/s) where that is
+// provably the same code, else the correctly rounded quotient for the whole chunk.
+template <bool E4M3>
+__device__ __forceinline__ uint2 quant_chunk(const float (&v)[8], const RowScale& rs) {
+  float y[8];
+  bool exact = rs.exact;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    y[j] = v[j] * rs.rs;
+    exact |= needs_exact<E4M3>(y[j]);
+  }
+  if (exact) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) y[j] = __fdiv_rn(v[j], rs.s);
+  }
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    lo |= code_of<E4M3>(y[j]) << (8 * j);
+    hi |= code_of<E4M3>(y[j + 4]) << (8 * j);
+  }
+  return make_uint2(lo, hi);
 }
 
 template <typename T, bool E4M3>
@@ -69,17 +128,12 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const T* __restrict__ x
   const float qmax = E4M3 ? 448.0f : 127.0f;
   const float s = (amax == 0.f) ? 1.0f : __fdiv_rn(amax, qmax);
   if (lane == 0) scales[row] = s;
+  const RowScale rs = row_scale(s);
   uint8_t* qr = q + static_cast<size_t>(row) * K;
   for (int c = lane * 8; c < K; c += 256) {
     float v[8];
     load8<T>(xr + c, v);
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t code = quant_code<E4M3>(v[i], s);
-      if (i < 4) lo |= code << (8 * i); else hi |= code << (8 * (i - 4));
-    }
-    *reinterpret_cast<uint2*>(qr + c) = make_uint2(lo, hi);
+    *reinterpret_cast<uint2*>(qr + c) = quant_chunk<E4M3>(v, rs);
   }
 }
 
@@ -147,6 +201,7 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const T* __restrict
   const float qmax = E4M3 ? 448.0f : 127.0f;
   const float sc = (amax == 0.f) ? 1.0f : __fdiv_rn(amax, qmax);
   if (sub == 0) scales[row] = sc;
+  const RowScale rs = row_scale(sc);
   uint8_t* qr = q + static_cast<size_t>(row) * K;
 #pragma unroll
   for (int i = 0; i < C; ++i) {
@@ -154,13 +209,7 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const T* __restrict
     if (c < K) {
       float v[8];
       raw[i].values(v);
-      uint32_t lo = 0, hi = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        lo |= quant_code<E4M3>(v[j], sc) << (8 * j);
-        hi |= quant_code<E4M3>(v[j + 4], sc) << (8 * j);
-      }
-      *reinterpret_cast<uint2*>(qr + c) = make_uint2(lo, hi);
+      *reinterpret_cast<uint2*>(qr + c) = quant_chunk<E4M3>(v, rs);
     }
   }
 }

@@ -38,26 +38,27 @@ def _hard_rows(M, K, seed):
     """Rows built to stress the quotient x / scale: per-row magnitudes 2^-60 .. 2^60, exact powers
     of two, small integers, repeated absmax values, and values on and next to the e4m3 rounding
     midpoints and the INT8 half-integers times the row scale (where a quotient one ulp off would
-    change the code)."""
+    change the code). The large kinds are placed first and the row's absmax taken after them, so
+    that the boundary values sit on boundaries of the scale the row actually gets."""
     rng = np.random.default_rng(seed)
     x = rng.normal(0, 1, size=(M, K)).astype(np.float32)
     mag = np.float32(2.0) ** rng.integers(-60, 61, size=(M, 1)).astype(np.float32)
     x *= mag
     kind = rng.integers(0, 5, size=(M, K))
+    x = np.where(kind == 2, np.float32(2.0) ** rng.integers(-8, 8, size=(M, K)).astype(np.float32) * mag, x)
+    x = np.where(kind == 3, rng.integers(-300, 300, size=(M, K)).astype(np.float32) * mag, x)
     amax = np.abs(x).max(axis=1, keepdims=True)
     scale = (amax / np.float32(448.0)).astype(np.float32)
     mids = ((quant.E4M3_VALUES[1:0x7E] + quant.E4M3_VALUES[2:0x7F]) / 2).astype(np.float32)
     pick = rng.integers(0, len(mids), size=(M, K))
-    nudge = rng.integers(-2, 3, size=(M, K)).astype(np.int32)
+    nudge = rng.integers(-3, 4, size=(M, K)).astype(np.int32)
     on_mid = (mids[pick] * scale).astype(np.float32)
     on_mid = (on_mid.view(np.int32) + nudge).view(np.float32)             # a few ulps either side
     x = np.where(kind == 1, on_mid, x)
-    x = np.where(kind == 2, np.float32(2.0) ** rng.integers(-8, 8, size=(M, K)).astype(np.float32) * mag, x)
-    x = np.where(kind == 3, rng.integers(-300, 300, size=(M, K)).astype(np.float32) * mag, x)
     # half-integers times the INT8 row scale (absmax / 127), a few ulps either side: INT8 rounding ties
     s8 = (amax / np.float32(127.0)).astype(np.float32)
     half = ((rng.integers(-127, 127, size=(M, K)) + 0.5).astype(np.float32) * s8).astype(np.float32)
-    half = (half.view(np.int32) + rng.integers(-2, 3, size=(M, K)).astype(np.int32)).view(np.float32)
+    half = (half.view(np.int32) + rng.integers(-3, 4, size=(M, K)).astype(np.int32)).view(np.float32)
     x = np.where(kind == 4, half, x)
     x[:, 0] = amax[:, 0]
     x[:, 1] = -amax[:, 0]
