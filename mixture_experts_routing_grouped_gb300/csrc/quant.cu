@@ -6,8 +6,9 @@
 // FP8-e4m3 variant uses absmax / 448 and a round-to-nearest-even, saturating
 // conversion. Scale and quotient are IEEE fp32 operations (no fast-math), so the
 // codes are exactly those of the same arithmetic done on the host; the quotient is
-// formed as x * RN(1/scale) wherever an error bound shows that gives the same code,
-// else by the correctly rounded division. An all-zero row gets scale 1 and codes 0.
+// bracketed by two products x * RN(1/scale) (1 -+ 2^-21), whose codes, where they
+// agree, are provably the code of the correctly rounded quotient; elsewhere it is
+// the correctly rounded division. An all-zero row gets scale 1 and codes 0.
 //
 // Rows of up to 2048 bf16 (1024 fp32) values are loaded once into the registers
 // of 8, 16 or 32 lanes (several rows per warp), and the absmax and the codes are
@@ -49,63 +50,107 @@ __device__ __forceinline__ uint32_t code_of(float r) {
   return static_cast<uint32_t>(static_cast<int>(rq)) & 0xffu;
 }
 
-// Whether y = x * RN(1/s) may round to another code than RN(x / s) does. With
-// u = 2^-24, RN(1/s) = (1/s)(1 + e1) and y = (x/s)(1 + e1)(1 + e2), |e1|, |e2| <= u, so
-// |y - x/s| < 2 ulp(x/s) and y, RN(x/s) are at most 2 ulps apart (one binade: the
-// boundaries below sit mid-binade). The two codes can then differ only where a
-// rounding boundary of the target lies within 2 ulps of y; the test takes 3.
-//  e4m3, |y| >= 2^-6: the boundaries are the midpoints 2^e (1 + (2m+1)/16), whose fp32
-//    encodings have bit 19 set and bits 18..0 clear; 0 < |y| < 2^-6 (e4m3 subnormals,
-//    whose boundaries are spread over several binades) always takes the exact path.
-//  INT8: the boundaries are the half-integers; |y - rint(y)| is exact, and 2^-14
-//    exceeds 3 ulps for every |y| < 128.
-template <bool E4M3>
-__device__ __forceinline__ bool needs_exact(float y) {
-  if (E4M3) {
-    const uint32_t a = __float_as_uint(y) & 0x7fffffffu;
-    return (a - 1u < 0x3c800000u - 1u) || ((a & 0xfffffu) - 0x7fffdu < 7u);
-  }
-  return fabsf(fabsf(y - rintf(y)) - 0.5f) <= 0x1p-14f;
-}
-
-// Per-row constants of the quotient: s, RN(1/s), and whether the product path is
-// valid for the row (s and 1/s normal, so that neither rounding step underflows
-// outside the e4m3 subnormal range, which is checked per value).
+// Per-row constants of the quotient. With u = 2^-24 and r = RN(1/s), the bracket
+// factors are r_lo = RN(r (1 - 8u)) and r_hi = RN(r (1 + 8u)); for z = x / s > 0,
+//   RN(x r_lo) <= z (1 + u)^3 (1 - 8u) < z (1 - u) <= RN(z)
+// and symmetrically RN(x r_hi) > RN(z) (mirrored for z < 0), each step a correctly
+// rounded fp32 operation of relative error at most u. Both codes (e4m3 round to
+// nearest even with saturation, and INT8 rint then clamp) are monotone in their
+// argument, so where the codes of RN(x r_lo) and RN(x r_hi) agree they are the code of
+// RN(z). Where they differ, a rounding boundary M lies between the two; if x = M s
+// exactly (fma(-M, s, x) == 0, no underflow for the rows' range of s) then RN(z) = M,
+// whose own conversion settles the tie; otherwise the value takes the correctly
+// rounded division. Rows with s outside [2^-100, 2^100] take the division throughout.
+// Below the fp32 normal range every bracket value and RN(z) has code +-0 with the
+// sign of x.
 struct RowScale {
-  float s, rs;
+  float s, lo, hi;
   bool exact;
 };
 
 __device__ __forceinline__ RowScale row_scale(float sc) {
   RowScale r;
+  const float rc = __frcp_rn(sc);
   r.s = sc;
-  r.rs = __frcp_rn(sc);
-  r.exact = !(sc >= 0x1p-125f && sc <= 0x1p125f);
+  r.lo = rc * (1.0f - 0x1p-21f);
+  r.hi = rc * (1.0f + 0x1p-21f);
+  r.exact = !(sc >= 0x1p-100f && sc <= 0x1p100f);
   return r;
 }
 
-// Codes of eight values x / s, packed little-endian: x * RN(1/s) where that is
-// provably the same code, else the correctly rounded quotient for the whole chunk.
+// Codes of two values x / s (value 0 in the low byte) from the bracket alone, and a
+// flag set where either value's bracket codes differ or the row takes the division.
 template <bool E4M3>
-__device__ __forceinline__ uint2 quant_chunk(const float (&v)[8], const RowScale& rs) {
-  float y[8];
-  bool exact = rs.exact;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    y[j] = v[j] * rs.rs;
-    exact |= needs_exact<E4M3>(y[j]);
+__device__ __forceinline__ uint32_t quant_pair_fast(float x0, float x1, const RowScale& rs, bool& flag) {
+  const float a0 = x0 * rs.lo, a1 = x1 * rs.lo;
+  const float b0 = x0 * rs.hi, b1 = x1 * rs.hi;
+  if (E4M3) {
+    const uint32_t cl = __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
+    flag = rs.exact || cl != __nv_cvt_float2_to_fp8x2(make_float2(b0, b1), __NV_SATFINITE, __NV_E4M3);
+    return cl;
   }
-  if (exact) {
+  const float l0 = rintf(a0), l1 = rintf(a1);
+  flag = rs.exact || l0 != rintf(b0) || l1 != rintf(b1);
+  return code_of<false>(l0) | (code_of<false>(l1) << 8);
+}
+
+// Codes of eight values, packed little-endian (value j in byte j); bit p of the
+// returned flags marks pair p (values 2p, 2p+1) for resolve_pair.
+template <bool E4M3>
+__device__ __forceinline__ uint2 quant_chunk_fast(const float (&v)[8], const RowScale& rs, uint32_t& flags) {
+  uint32_t c[4];
+  flags = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) y[j] = __fdiv_rn(v[j], rs.s);
+  for (int p = 0; p < 4; ++p) {
+    bool f;
+    c[p] = quant_pair_fast<E4M3>(v[2 * p], v[2 * p + 1], rs, f);
+    flags |= static_cast<uint32_t>(f) << p;
   }
-  uint32_t lo = 0, hi = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    lo |= code_of<E4M3>(y[j]) << (8 * j);
-    hi |= code_of<E4M3>(y[j + 4]) << (8 * j);
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// Exact code of one value x / s. Where the bracket codes differ, M is the boundary
+// between them: for e4m3 the bracket's low end rounded to 4 fractional mantissa bits
+// (every e4m3 midpoint has at most that many), for INT8 the half-integer between the
+// two. x = M s exactly (fma(-M, s, x) == 0) makes RN(x / s) = M, whose conversion
+// settles the tie; anything else takes the correctly rounded division.
+template <bool E4M3>
+__device__ __forceinline__ uint32_t code_exact(float x, const RowScale& rs) {
+  const float a = x * rs.lo, b = x * rs.hi;
+  float m;
+  if (E4M3) m = __uint_as_float((__float_as_uint(a) + 0x40000u) & 0xfff80000u);
+  else m = (rintf(a) + rintf(b)) * 0.5f;
+  if (!rs.exact) {
+    const uint32_t ca = code_of<E4M3>(a);
+    if (ca == code_of<E4M3>(b)) return ca;
+    if (fmaf(-m, rs.s, x) == 0.0f) return code_of<E4M3>(m);
   }
-  return make_uint2(lo, hi);
+  return code_of<E4M3>(__fdiv_rn(x, rs.s));
+}
+
+template <typename T>
+__device__ __forceinline__ void load2(const T* p, float& v0, float& v1);
+template <>
+__device__ __forceinline__ void load2<float>(const float* p, float& v0, float& v1) {
+  const float2 a = __ldg(reinterpret_cast<const float2*>(p));
+  v0 = a.x;
+  v1 = a.y;
+}
+template <>
+__device__ __forceinline__ void load2<__nv_bfloat16>(const __nv_bfloat16* p, float& v0, float& v1) {
+  const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(p));
+  v0 = __uint_as_float(w << 16);
+  v1 = __uint_as_float(w & 0xffff0000u);
+}
+
+// Rewrites the two codes at column c (even) of a row whose fast codes were stored
+// earlier by this thread, re-reading the two values (cached).
+template <typename T, bool E4M3>
+__device__ __forceinline__ void resolve_pair(const T* xr, uint8_t* qr, int c, const RowScale& rs) {
+  float v0, v1;
+  load2<T>(xr + c, v0, v1);
+  const uint32_t code = code_exact<E4M3>(v0, rs) | (code_exact<E4M3>(v1, rs) << 8);
+  *reinterpret_cast<uint16_t*>(qr + c) = static_cast<uint16_t>(code);
 }
 
 template <typename T, bool E4M3>
@@ -133,7 +178,13 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const T* __restrict__ x
   for (int c = lane * 8; c < K; c += 256) {
     float v[8];
     load8<T>(xr + c, v);
-    *reinterpret_cast<uint2*>(qr + c) = quant_chunk<E4M3>(v, rs);
+    uint32_t f;
+    *reinterpret_cast<uint2*>(qr + c) = quant_chunk_fast<E4M3>(v, rs, f);
+    while (f) {
+      const int p = __ffs(f) - 1;
+      f &= f - 1;
+      resolve_pair<T, E4M3>(xr, qr, c + 2 * p, rs);
+    }
   }
 }
 
@@ -172,6 +223,7 @@ template <typename T, bool E4M3, int L, int C>
 __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const T* __restrict__ x, int M, int K,
                                                              uint8_t* __restrict__ q, float* __restrict__ scales,
                                                              const int* __restrict__ rows_dev) {
+  static_assert(4 * C <= 32, "one flag bit per pair of a lane's chunks");
   const int gl = blockIdx.x * blockDim.x + threadIdx.x;
   const int row = gl / L;
   const int sub = gl & (L - 1);
@@ -203,14 +255,23 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const T* __restrict
   if (sub == 0) scales[row] = sc;
   const RowScale rs = row_scale(sc);
   uint8_t* qr = q + static_cast<size_t>(row) * K;
+  uint32_t flagged = 0;  // bit 4 i + p: pair p of chunk i needs resolve_pair
 #pragma unroll
   for (int i = 0; i < C; ++i) {
     const int c = (sub + L * i) * 8;
     if (c < K) {
       float v[8];
       raw[i].values(v);
-      *reinterpret_cast<uint2*>(qr + c) = quant_chunk<E4M3>(v, rs);
+      uint32_t f;
+      *reinterpret_cast<uint2*>(qr + c) = quant_chunk_fast<E4M3>(v, rs, f);
+      flagged |= f << (4 * i);
     }
+  }
+  // One copy of the exact path, outside the unrolled loop: rare pairs only.
+  while (flagged) {
+    const int b = __ffs(flagged) - 1;
+    flagged &= flagged - 1;
+    resolve_pair<T, E4M3>(xr, qr, (sub + L * (b >> 2)) * 8 + 2 * (b & 3), rs);
   }
 }
 
