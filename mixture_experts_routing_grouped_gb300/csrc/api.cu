@@ -3,6 +3,7 @@
 #include "common.cuh"
 
 #include <mutex>
+#include <map>
 #include <set>
 #include <utility>
 
@@ -26,13 +27,14 @@ moe_status_t launch_status() { return cudaGetLastError() == cudaSuccess ? MOE_OK
 
 bool ensure_smem_attr(const void* func, int bytes) {
   static std::mutex mu;
-  static std::set<std::pair<const void*, int>> done;
+  static std::map<std::pair<const void*, int>, int> set_bytes;  // largest limit set per (kernel, device)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   std::lock_guard<std::mutex> g(mu);
-  if (done.count({func, dev})) return true;
+  auto it = set_bytes.find({func, dev});
+  if (it != set_bytes.end() && it->second >= bytes) return true;
   if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
-  done.insert({func, dev});
+  set_bytes[{func, dev}] = bytes;
   return true;
 }
 

@@ -35,7 +35,8 @@ int num_sms();
 
 moe_status_t launch_status();
 
-// Raises a kernel's dynamic shared memory limit once per (kernel, device).
+// Raises a kernel's dynamic shared memory limit to at least `bytes` (the largest
+// limit set so far is remembered per (kernel, device)).
 bool ensure_smem_attr(const void* func, int bytes);
 
 }  // namespace moe

@@ -17,7 +17,8 @@ def _gpu():
 
 @pytest.mark.parametrize("qdt", [torch.int8, torch.float8_e4m3fn])
 @pytest.mark.parametrize("xdt", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("M,K", [(1, 8), (37, 264), (2048, 4096)])
+# (20000, 768) and (5000, 2048): several rows per warp of the persistent bf16 kernel
+@pytest.mark.parametrize("M,K", [(1, 8), (37, 264), (2048, 4096), (20000, 768), (5000, 2048)])
 def test_quant_rows(qdt, xdt, M, K):
     import mixture_experts_routing_grouped_gb300 as moe
     x = synth.normal((M, K), 99, M + K, 1.0, xdt, "cuda")
@@ -67,7 +68,7 @@ def _hard_rows(M, K, seed):
 
 @pytest.mark.parametrize("qdt", [torch.int8, torch.float8_e4m3fn])
 @pytest.mark.parametrize("xdt", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("M,K", [(4096, 1024), (1024, 2048), (128, 4104)])
+@pytest.mark.parametrize("M,K", [(4096, 1024), (1024, 2048), (128, 4104), (12000, 768)])
 def test_quant_rows_hard_values(qdt, xdt, M, K):
     import mixture_experts_routing_grouped_gb300 as moe
     xt = torch.from_numpy(_hard_rows(M, K, M + K)).to(xdt)
