@@ -288,7 +288,8 @@ __global__ void __launch_bounds__(gemm_threads<F8>(), 1)
       } else {
         // The TMEM load of the next 32 columns is issued as soon as the current
         // one has landed, so that it overlaps this chunk's scaling, staging and
-        // atomics (FP8 tiles have half the main loop to hide the combine behind).
+        // atomics; the token row is shuffled per row (bf16 tiles have the longer
+        // main loop, which hides this combine).
         constexpr int kCh = kBN / 32 / kParts;  // 32-column chunks per warp
         const int c0 = chalf * kCh;
         uint32_t d[2][32];
@@ -296,24 +297,14 @@ __global__ void __launch_bounds__(gemm_threads<F8>(), 1)
   #pragma unroll
         for (int ci = 0; ci < kCh; ++ci) {
           const int c = c0 + ci;
-          float4 cs[8];
-          if constexpr (F8) {
-            const float4* swc =
-                reinterpret_cast<const float4*>(args.sw + static_cast<size_t>(e_of_tile) * args.H + nt * kBN + c * 32);
-  #pragma unroll
-            for (int q = 0; q < 8; ++q) cs[q] = __ldg(swc + q);
-          }
           ptx::tmem_ld_wait();
           if (ci + 1 < kCh) ptx::tmem_ld32(tbase + (c + 1) * 32, d[(ci + 1) & 1]);
           const uint32_t* dc = d[ci & 1];
           float4 srow[8];
   #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 k = F8 ? make_float4(w * cs[q].x, w * cs[q].y, w * cs[q].z, w * cs[q].w)
-                                : make_float4(w, w, w, w);
-            srow[q] = make_float4(k.x * __uint_as_float(dc[4 * q]), k.y * __uint_as_float(dc[4 * q + 1]),
-                                  k.z * __uint_as_float(dc[4 * q + 2]), k.w * __uint_as_float(dc[4 * q + 3]));
-          }
+          for (int q = 0; q < 8; ++q)
+            srow[q] = make_float4(w * __uint_as_float(dc[4 * q]), w * __uint_as_float(dc[4 * q + 1]),
+                                  w * __uint_as_float(dc[4 * q + 2]), w * __uint_as_float(dc[4 * q + 3]));
   #pragma unroll
           for (int q = 0; q < 8; ++q) stg[lane * 8 + (q ^ (lane & 7))] = srow[q];
           __syncwarp();
