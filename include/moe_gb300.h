@@ -171,6 +171,11 @@ MOE_API moe_status_t moe_fused_forward(const void* x, const float* gating, const
  *  256, I a multiple of 128); ws of at least moe_fused_forward_fp8_workspace_size(...)
  *  bytes, 256-byte aligned and zero-filled before its first use. Every problem size
  *  uses the 128-row block layout (no decode-specific kernel for this dtype).
+ *  Streams: x is quantised on a second stream of the library's own (one per host
+ *  thread and device, created at the first call and kept), forked from `stream` by an
+ *  event at the start of the call and joined back into it before the gate_up GEMM,
+ *  so that it overlaps routing and align; everything stays ordered on `stream` and the
+ *  call can be captured into a CUDA graph. Make the first call outside a capture.
  */
 MOE_API size_t moe_fused_forward_fp8_workspace_size(int T, int H, int I, int E, int topk);
 MOE_API moe_status_t moe_fused_forward_fp8(const void* x, const float* gating, const void* w_gate_up,
@@ -219,8 +224,9 @@ MOE_API moe_status_t moe_fused_forward_noalloc(const void* x, const float* gatin
  * 4 down GEMM, 5 cast to bf16 (n >= 6 records all). The fp32 accumulator of the
  * down pass is cleared inside step 3 (prefill kernels) or step 1 (decode
  * kernels). moe_fused_forward_fp8 records events[0] before routing and after
- * 1 routing, 2 align, 3 quantisation of x, 4 gate_up GEMM, 5 quantisation of h,
- * 6 down GEMM, 7 cast (n = 8 records all). The events are cudaEvent_t handles
+ * 1 routing, 2 align, 3 the join with the quantisation of x (which runs beside
+ * steps 1-2 on a second stream: interval 3 is the part of it left exposed),
+ * 4 gate_up GEMM, 5 quantisation of h, 6 down GEMM, 7 cast (n = 8 records all). The events are cudaEvent_t handles
  * owned by the caller. events = NULL or n = 0 switches the recording off.
  */
 MOE_API void moe_set_stage_events(void* const* events, int n);

@@ -160,6 +160,36 @@ Fp8Layout fp8_layout(int T, int H, int I, int E, int topk) {
   return L;
 }
 
+// A second stream per (host thread, device), with a fork and a join event, on which
+// the FP8 forward quantises x while routing and align (small, latency-bound launches
+// that leave most SMs idle) run on the caller's stream. Forked from and joined back
+// into the caller's stream by events, so the call stays ordered on that stream and
+// capturable into a CUDA graph. Created on first use and kept; null if creation
+// failed (the work then stays on the caller's stream).
+struct SideStream {
+  cudaStream_t st = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool tried = false;
+};
+
+SideStream* side_stream() {
+  constexpr int kMaxDevices = 64;
+  thread_local SideStream per_device[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream& ss = per_device[dev];
+  if (!ss.tried) {
+    ss.tried = true;
+    if (cudaStreamCreateWithFlags(&ss.st, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      ss.st = nullptr;
+    }
+  }
+  return ss.st ? &ss : nullptr;
+}
+
 thread_local cudaEvent_t g_stage_events[8];
 thread_local int g_num_stage_events = 0;
 
@@ -315,6 +345,16 @@ extern "C" moe_status_t moe_fused_forward_fp8(const void* x, const float* gating
   const int cap = L.base.cap;
 
   stage_mark(0, s);
+  // x's per-token codes depend on x alone: quantised on the side stream while routing
+  // and align run here, joined before gate_up reads them.
+  SideStream* side = side_stream();
+  if (side) {
+    if (cudaEventRecord(side->fork, s) != cudaSuccess || cudaStreamWaitEvent(side->st, side->fork, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    st = launch_quant_rows_e4m3_bf16(static_cast<const __nv_bfloat16*>(x), T, H, qx, sx, nullptr, side->st);
+    if (st != MOE_OK) return st;
+    if (cudaEventRecord(side->join, side->st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   st = launch_grouped_topk(gating, T, E, num_expert_group, topk_group, topk, scoring, renormalize,
                            routed_scaling_factor, topk_weights, topk_ids, s, nullptr, H, nullptr, 0);
   if (st != MOE_OK) return st;
@@ -323,8 +363,12 @@ extern "C" moe_status_t moe_fused_forward_fp8(const void* x, const float* gating
                     err, s, sorted_tok, topk, tile_counter);
   if (st != MOE_OK) return st;
   stage_mark(2, s);
-  st = launch_quant_rows_e4m3_bf16(static_cast<const __nv_bfloat16*>(x), T, H, qx, sx, nullptr, s);
-  if (st != MOE_OK) return st;
+  if (side) {
+    if (cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    st = launch_quant_rows_e4m3_bf16(static_cast<const __nv_bfloat16*>(x), T, H, qx, sx, nullptr, s);
+    if (st != MOE_OK) return st;
+  }
   stage_mark(3, s);
   st = launch_gemm_gate_up_pairs_fp8(qx, sx, static_cast<const uint8_t*>(w_gate_up), scales_gate_up, sorted_tok,
                                      offsets, h, err, H, I, E, y_acc, static_cast<size_t>(T) * H, tile_counter, s);
