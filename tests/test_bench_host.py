@@ -1,0 +1,56 @@
+"""Host logic of bench.py that needs no GPU: the clock sampler's parsing of
+nvidia-smi's CSV and its selection of the samples inside a time window (the timed
+steps, and the sustained window after them)."""
+import datetime
+
+import bench
+
+
+class _Done:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        pass
+
+
+def _sampler_with(tmp_path, lines):
+    cs = bench.ClockSampler(0)
+    cs.path = tmp_path / "clocks.csv"
+    cs.path.write_text("\n".join(lines) + "\n")
+    cs.proc = _Done()
+    cs.fh = open(cs.path, "a")
+    return cs
+
+
+def _line(t, sm, power_cap=False, thermal=False):
+    ts = t.strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    na, act = "Not Active", "Active"
+    return (f"{ts}, 0, {sm}, 2070, 900.00, 0x0, {na}, {na}, {act if thermal else na}, "
+            f"{act if power_cap else na}")
+
+
+def test_samples_are_selected_by_window(tmp_path):
+    t0 = datetime.datetime(2026, 1, 1, 12, 0, 0)
+    ms = lambda k: t0 + datetime.timedelta(milliseconds=k)
+    lines = [_line(ms(10 * i), 2070 if i < 5 else 1800, power_cap=(i == 7)) for i in range(10)]
+    lines.insert(3, "garbage line")
+    lines.append("2026/01/01 12:00:01.000, 0, [N/A], 2070, 0, 0x0, x, x, x, x")
+    rows = _sampler_with(tmp_path, lines).stop()
+    assert len(rows) == 10                                  # malformed lines skipped
+    first = bench.ClockSampler.summary(rows, ms(0), ms(45))
+    assert first == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 5}
+    late = bench.ClockSampler.summary(rows, ms(50), ms(95))
+    assert late["sm_mhz"] == 1800.0 and late["reasons"] == ["sw_power_cap"] and late["samples"] == 5
+    assert bench.ClockSampler.summary(rows, ms(500), ms(600))["samples"] == 0
+
+
+def test_thermal_reasons_are_reported(tmp_path):
+    t0 = datetime.datetime(2026, 1, 1, 12, 0, 0)
+    rows = _sampler_with(tmp_path, [_line(t0, 1500, thermal=True)]).stop()
+    s = bench.ClockSampler.summary(rows, t0, t0)
+    assert s["reasons"] == ["sw_thermal_slowdown"] and s["sm_mhz"] == 1500.0
+
+
+def test_no_sampler_gives_no_rows():
+    assert bench.ClockSampler(0).stop() is None
