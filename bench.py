@@ -25,6 +25,7 @@ import pathlib
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = pathlib.Path(__file__).resolve().parent
@@ -59,12 +60,15 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = ROOT / "gpurun_out" / f"clocks_rank{gpu_index}.csv"
+        # The raw samples go to $MOE_BENCH_CLOCKS_DIR when it is set (to keep them), else
+        # to the system's temporary directory.
+        out = os.environ.get("MOE_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = pathlib.Path(out) / f"moe_bench_clocks_gpu{gpu_index}_{os.getpid()}.csv"
 
     def start(self, wait_s: float = 3.0):
         """Starts the sampler and returns once it has written its first sample (or after wait_s)."""
         try:
-            self.path.parent.mkdir(exist_ok=True)
+            self.path.parent.mkdir(parents=True, exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "10"],
@@ -116,6 +120,22 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- helpers
+def max_over_ranks(torch, value: float, device) -> float:
+    """The largest `value` over the ranks of the default process group (`value` itself when
+    no group is initialised). Every rank must call it: it is a collective."""
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: the tokens every rank processed over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 def kernel_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source."""
     p = ROOT / "profiles" / "traffic.json"
@@ -249,11 +269,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
     stage_names = ["routing", "align", "gemm_gate_up", "gemm_down", "cast"]
     stage_ms = {n: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
                 for i, n in enumerate(stage_names)}
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, statistics.mean(step_ms), dev)
     err = moe.moe_check_device_error(ws)
     if err:
         raise RuntimeError(f"device error word {err:#x}")
@@ -280,11 +296,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
         b.synchronize()
         if k >= args.warmup:
             e2e.append(a.elapsed_time(b))
-    e2e_ms = statistics.mean(e2e)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(torch, statistics.mean(e2e), dev)
     h2d = xh.numel() * 2 + gh.numel() * 4
     d2h = yh.numel() * 2 + twh.numel() * 4 + idh.numel() * 4
 
@@ -299,7 +311,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
 
     result = {
         "metric": METRIC,
-        "value": round(world * cfg.T / (ms * 1e-3), 1),
+        "value": round(job_tokens_per_s(cfg.T, world, ms), 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
@@ -320,7 +332,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
         "layer_tflops": round(layer_tflops, 1),
         "layer_frac_bf16_peak": round(layer_tflops / peak, 4),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-        "e2e": {"value": round(world * cfg.T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(cfg.T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": 6 * K,  # per step: routing, align histogram, align scan + scatter, gate_up, down, cast
         "clocks": clk,

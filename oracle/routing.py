@@ -33,7 +33,9 @@ def scores(logits: np.ndarray, scoring_func: str) -> np.ndarray:
         ex = np.exp(x - m)
         return ex / ex.sum(axis=-1, keepdims=True)
     if scoring_func == "sigmoid":
-        return 1.0 / (1.0 + np.exp(-x))
+        # exp(-x) overflows to inf for x below about -709, which gives the limit 0 exactly.
+        with np.errstate(over="ignore"):
+            return 1.0 / (1.0 + np.exp(-x))
     raise ValueError(f"unknown scoring_func {scoring_func!r}")
 
 

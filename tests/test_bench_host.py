@@ -1,6 +1,7 @@
 """Host logic of bench.py that needs no GPU: the clock sampler's parsing of
 nvidia-smi's CSV and its selection of the samples inside a time window (the timed
-steps, and the sustained window after them)."""
+steps, and the sustained window after them), and the max-over-ranks timing of
+replicas, run as two gloo ranks on CPU."""
 import datetime
 
 import bench
@@ -54,3 +55,45 @@ def test_thermal_reasons_are_reported(tmp_path):
 
 def test_no_sampler_gives_no_rows():
     assert bench.ClockSampler(0).stop() is None
+
+
+def _rank_main(rank, world, port, step_ms, out):
+    import os
+    import torch
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = bench.max_over_ranks(torch, step_ms[rank], torch.device("cpu"))
+        out[rank] = (ms, bench.job_tokens_per_s(4096, world, ms))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replica_timing_takes_the_slowest_rank():
+    """Two gloo ranks on CPU with different step times: both see the slower one, and the job's
+    throughput counts both ranks' tokens over it (the N > 1 bookkeeping of the bench)."""
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    step_ms = [0.35, 0.5]
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, step_ms, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    for r in range(2):
+        ms, tps = out[r]
+        assert ms == 0.5
+        assert abs(tps - 2 * 4096 / 0.5e-3) < 1e-6 * tps
+
+
+def test_single_process_timing_is_unchanged():
+    import torch
+    assert bench.max_over_ranks(torch, 0.25, torch.device("cpu")) == 0.25
+    assert bench.job_tokens_per_s(4096, 1, 0.25) == 4096 / 0.25e-3
