@@ -237,7 +237,6 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   const Plan plan = choose_plan(T, E, topk);
   const FusedLayout L = fused_layout(T, H, I, E, topk, plan.block_m);
   if (!ws || ws_bytes < moe_fused_forward_workspace_size(T, H, I, E, topk) || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
-  if (T == 0) return MOE_OK;
 
   cudaStream_t s = as_stream(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);

@@ -27,7 +27,7 @@ def _run(logits_np, k, renorm, G, kg, scoring, rsf):
     assert_weights_close(w.cpu().numpy(), rw)
 
 
-@pytest.mark.parametrize("T", [1, 128, 4096, 16384])
+@pytest.mark.parametrize("T", [1, 128, 4096, 16384, 65536])
 @pytest.mark.parametrize("scoring", ["softmax", "sigmoid"])
 def test_routing_workload(T, scoring):
     cfg = synth.routing_config(T, scoring)
