@@ -1,6 +1,7 @@
 """The C-ABI library builds, loads and exports every declared symbol; host-side
 validation and size queries behave as documented. No GPU needed: nothing here
-launches a kernel."""
+launches a kernel. Every call below is one that the documented checks reject (or
+find empty) before any launch, so no fake pointer here ever reaches a kernel."""
 import ctypes
 import pathlib
 import re
@@ -118,3 +119,58 @@ def test_fused_fp8_validation_and_sizes(L):
     assert need > L.moe_fused_forward_workspace_size(64, 512, 256, 8, 2)
     assert f(*args(512, 256, need - 1)) == 3
     assert f(*args(512, 256, need, ctypes.c_void_p(0x10010))) == 3  # workspace not 256-byte aligned
+
+
+def test_gmm_lowp_validation(L):
+    f = L.gmm_lowp
+    I8, E4, BF, F32 = 2, 3, 0, 1
+    ws = 1 << 30
+
+    def call(M=256, K=256, N=256, E=4, in_dt=E4, out_dt=BF, inp=FAKE, w=FAKE, sx=FAKE, sw=FAKE, off=FAKE,
+             sz=FAKE, out=FAKE, wsp=FAKE, wsb=ws):
+        return f(inp, w, sx, sw, off, sz, out, M, K, N, E, in_dt, out_dt, wsp, wsb, None)
+
+    assert call(in_dt=BF) == 1                          # inputs must be int8 or e4m3
+    assert call(out_dt=I8) == 1                         # output must be bf16 or fp32
+    assert call(E=0) == 1 and call(E=2048) == 1         # 1 <= E <= 1024
+    assert call(M=-1) == 1 and call(K=0) == 1 and call(N=0) == 1
+    assert call(w=None) == 1 and call(sw=None) == 1 and call(off=None) == 1 and call(sz=None) == 1
+    assert call(inp=None) == 1 and call(sx=None) == 1 and call(out=None) == 1
+    assert call(K=200) == 2 and call(N=200) == 2       # K and N in whole 128-wide tiles
+    assert call(inp=ctypes.c_void_p(0x10008)) == 2      # operands 16-byte aligned
+    assert call(wsp=None) == 3
+    assert call(wsp=ctypes.c_void_p(0x10010)) == 3      # workspace 256-byte aligned
+    need8 = L.gmm_lowp_workspace_size(256, 256, 256, 4)
+    assert call(in_dt=I8, wsb=need8 - 1) == 3           # INT8 needs room for the widened codes
+    assert call(M=0, inp=None, sx=None, out=None) == 0  # no rows: nothing to do
+
+
+def test_quant_validation(L):
+    f = L.moe_quant_per_token
+    BF, F32, I8, E4 = 0, 1, 2, 3
+    assert f(FAKE, I8, 4, 64, E4, FAKE, FAKE, None) == 1    # x must be bf16 or fp32
+    assert f(FAKE, BF, 4, 64, BF, FAKE, FAKE, None) == 1    # codes must be int8 or e4m3
+    assert f(FAKE, BF, -1, 64, I8, FAKE, FAKE, None) == 1
+    assert f(FAKE, BF, 4, 0, I8, FAKE, FAKE, None) == 1
+    assert f(None, BF, 4, 64, I8, FAKE, FAKE, None) == 1
+    assert f(FAKE, BF, 4, 64, I8, FAKE, None, None) == 1
+    assert f(FAKE, BF, 4, 60, I8, FAKE, FAKE, None) == 2     # K a multiple of 8
+    assert f(ctypes.c_void_p(0x10008), BF, 4, 64, I8, FAKE, FAKE, None) == 2  # x 16-byte aligned
+    assert f(FAKE, F32, 4, 64, I8, ctypes.c_void_p(0x10004), FAKE, None) == 2  # codes 8-byte aligned
+    assert f(None, BF, 0, 64, I8, None, None, None) == 0     # no rows: nothing to do
+
+
+def test_check_device_error_needs_its_arguments(L):
+    code = ctypes.c_int(0)
+    assert L.moe_check_device_error(None, ctypes.byref(code), None) == 1
+    assert L.moe_check_device_error(FAKE, None, None) == 1
+
+
+def test_noalloc_rejects_on_the_host(L):
+    """The allocation-free forward refuses, before touching any device, a problem whose
+    workspace exceeds its fixed scratch array, and arguments that size no workspace."""
+    f = L.moe_fused_forward_noalloc
+    T, H, I, E, k = 4096, 2048, 768, 128, 8
+    assert L.moe_fused_forward_workspace_size(T, H, I, E, k) > 64 * 1024 * 1024
+    assert f(FAKE, FAKE, FAKE, FAKE, T, H, I, E, 1, 1, k, 0, 1, 1.0, FAKE, FAKE, FAKE, None) == 3
+    assert f(FAKE, FAKE, FAKE, FAKE, 64, 0, 256, 8, 1, 1, 2, 0, 1, 1.0, FAKE, FAKE, FAKE, None) == 1
