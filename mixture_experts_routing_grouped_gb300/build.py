@@ -7,6 +7,7 @@ rebuild when nothing changed.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import hashlib
 import os
 import pathlib
@@ -46,11 +47,27 @@ def _stamp() -> str:
 
 
 def build(verbose: bool = False, force: bool = False) -> pathlib.Path:
-    stamp_file = BUILD / "stamp"
+    """Builds the library unless the stamp shows it current. Processes that build at the
+    same time (one per GPU under torchrun, parallel test workers) take turns on a lock
+    file, so one compiles and the others find the stamp current."""
     stamp = _stamp()
-    if not force and LIB.exists() and stamp_file.exists() and stamp_file.read_text() == stamp:
+    if not force and _current(stamp):
         return LIB
     BUILD.mkdir(exist_ok=True)
+    with open(BUILD / "lock", "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and _current(stamp):
+            return LIB
+        return _build_locked(stamp, verbose)
+
+
+def _current(stamp: str) -> bool:
+    stamp_file = BUILD / "stamp"
+    return LIB.exists() and stamp_file.exists() and stamp_file.read_text() == stamp
+
+
+def _build_locked(stamp: str, verbose: bool) -> pathlib.Path:
+    stamp_file = BUILD / "stamp"
     nvcc = _nvcc()
 
     def compile_one(src: pathlib.Path) -> pathlib.Path:
