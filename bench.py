@@ -609,10 +609,11 @@ def cpu_baseline(cfg, budget_s: float = 12.0):
                       f"one run of {dt:.2f} s"}
 
 
-def run_reference(args, rank, world):
+def run_reference(args, rank, world, cfg=None, n: int = 256):
+    """The reference arm: the oracle on the first n tokens of the workload per step."""
     import synth
-    cfg = synth.prefill_config()
-    n = 256
+    cfg = cfg or synth.prefill_config()
+    n = min(n, cfg.T)
     x64, g32, w1, w2 = oracle_inputs(cfg, n)
     for _ in range(args.warmup):
         oracle_layer_step(cfg, x64, g32, w1, w2)

@@ -97,3 +97,30 @@ def test_single_process_timing_is_unchanged():
     import torch
     assert bench.max_over_ranks(torch, 0.25, torch.device("cpu")) == 0.25
     assert bench.job_tokens_per_s(4096, 1, 0.25) == 4096 / 0.25e-3
+
+
+_CONTRACT = {
+    "metric": str, "value": float, "unit": str, "n_gpus": int, "steps": int, "warmup": int,
+    "ms_per_step": float, "higher_is_better": bool, "scaling": str, "dtype": str, "data": str,
+    "config": dict, "cpu_baseline": dict, "e2e": dict,
+}
+
+
+def test_reference_arm_prints_the_contract_line():
+    """The reference arm (the oracle on host cores) runs without a GPU: its JSON line carries
+    every key of the bench contract, on a small workload here."""
+    import argparse
+    import json
+    import synth
+    args = argparse.Namespace(steps=2, warmup=3)
+    line = json.loads(json.dumps(bench.run_reference(args, 0, 1, cfg=synth.tiny_config(), n=16)))
+    for key, typ in _CONTRACT.items():
+        assert isinstance(line[key], typ), key
+    assert line["impl"] == "reference" and line["vs_baseline"] is None
+    assert line["config"]["workload"] == synth.tiny_config().name
+    assert line["metric"] == bench.METRIC and line["unit"] == "tokens/s" and line["higher_is_better"]
+    assert line["value"] > 0 and line["ms_per_step"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["cpu_baseline"]["cores"] >= 1 and "16 of 64 tokens" in line["cpu_baseline"]["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
