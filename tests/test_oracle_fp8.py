@@ -10,6 +10,10 @@
    that 3-bit-mantissa operands allow of the exact forward.
 3. Power-of-two equivariance: doubling the scale of one down-projection output
    channel doubles that output column exactly and leaves the others unchanged.
+4. A hand-worked token whose h row is held in bfloat16 before its per-row e4m3
+   quantisation: the bf16 rounding moves one value onto an e4m3 midpoint (ties to
+   even), so the output differs from the one without the bf16 step or without the
+   quantisation of h.
 """
 import numpy as np
 
@@ -92,3 +96,37 @@ def test_fp8_forward_down_channel_scale_equivariance():
     y1, _, _ = moe.fused_forward_fp8(x, gating, *args, s2b, k, True)
     assert np.array_equal(y1[:, 5], 2.0 * y0[:, 5])
     assert np.array_equal(np.delete(y1, 5, axis=1), np.delete(y0, 5, axis=1))
+
+
+E4M3_ONE, E4M3_448 = 0x38, 0x7E   # codes of 1.0 (0 0111 000) and 448 (0 1111 110)
+
+
+def test_fp8_token_with_h_held_in_bf16_worked_by_hand():
+    # x = [448, 1, 0, 0]: scale 1, dequantised x exactly [448, 1, 0, 0]. Only column 1 of
+    # the gate_up weights is non-zero (code 1.0), so g and u are the channel scales:
+    # gate channels 64, 64 (silu(64) == 64 in float64); up channels 6.125 and
+    # 3809/2^18, giving h = [392, 3809/4096] exactly.
+    # bf16(h) = [392, 238/256]; its row scale is 392/448 = 0.875 (exact), the quotients
+    # are 448 and 1.0625, the midpoint of the e4m3 values 1 and 1.125: ties to even
+    # give code 1.0, i.e. h dequantised [392, 0.875]. The down weights pick h[1] for
+    # output 0 (code 1.0, scale 1) with route weight 1: y[0] = 0.875 exactly.
+    # Without the bf16 step the quotient is 1.06278 -> 1.125 -> y[0] = 0.984375; without
+    # quantising h, y[0] = 3809/4096.
+    H, I = 4, 2
+    x = np.array([448.0, 1.0, 0.0, 0.0], dtype=np.float32)
+    q1 = np.zeros((2 * I, H), dtype=np.uint8)
+    q1[:, 1] = E4M3_ONE
+    s1 = np.array([64.0, 64.0, 6.125, 3809.0 / 2 ** 18], dtype=np.float32)
+    q2 = np.zeros((H, I), dtype=np.uint8)
+    q2[0, 1] = E4M3_ONE
+    s2 = np.ones(H, dtype=np.float32)
+    y = moe.token_outputs_fp8(x, [q1], [s1], [q2], [s2], np.array([1.0], dtype=np.float32))
+    assert y.tolist() == [0.875, 0.0, 0.0, 0.0]
+
+
+def test_e4m3_zero_row_gets_scale_one():
+    x = np.zeros((2, 64), dtype=np.float32)
+    x[1, 5] = -3.0
+    c, s = quant.quant_rows_e4m3(x)
+    assert s[0] == 1.0 and np.all(c[0] == 0)
+    assert s[1] == np.float32(3.0) / np.float32(448.0) and c[1, 5] == 0x80 | E4M3_448

@@ -61,6 +61,87 @@ def test_int8_quant_matches_article_recipe_in_torch():
     assert np.array_equal(s, scale.squeeze(1).numpy())
 
 
+def test_int8_ties_round_half_to_even():
+    # absmax 127 gives the scale 1 exactly (254 gives 2): every quotient below is an exact
+    # half-integer, and the article's torch.round sends it to the even neighbour, which is
+    # also what Python's round() does.
+    halves = [0.5, 1.5, 2.5, -2.5, -3.5, 63.5, 126.5, -126.5]
+    x = np.array([[127.0] + halves, [254.0] + [2 * h for h in halves]], dtype=np.float32)
+    q, s = quant.quant_rows_int8(x)
+    assert list(s) == [1.0, 2.0]
+    want = [127] + [round(h) for h in halves]
+    assert q[0].tolist() == want and q[1].tolist() == want
+
+
+def test_int8_quotient_is_rounded_to_fp32_first():
+    # The article's recipe divides in float32: where the exact quotient lies just off a
+    # half-integer but its float32 rounding lands on it (or across it), the code follows
+    # the float32 quotient. Rows are built from such values, and the torch recipe decides.
+    rng = np.random.default_rng(4)
+    rows, n_differ = [], 0
+    while len(rows) < 8:
+        amax = np.float32(rng.uniform(1.0, 2.0))
+        s32 = np.float32(amax / np.float32(127.0))
+        vals = []
+        for k in range(127):
+            base = np.float32((k + 0.5) * np.float64(s32))
+            for d in (-2, -1, 0, 1, 2):
+                v = base
+                for _ in range(abs(d)):
+                    v = np.nextafter(v, np.float32(np.inf if d > 0 else -np.inf), dtype=np.float32)
+                exact = np.float64(v) / np.float64(s32)
+                if np.rint(np.float32(v / s32)) != np.rint(exact):
+                    vals.append(v)
+        if vals:
+            n_differ += len(vals)
+            rows.append(np.array([amax] + vals[:63] + [0.0] * (63 - len(vals[:63])), dtype=np.float32))
+    x = np.stack(rows)
+    w = torch.from_numpy(x)
+    scale = w.abs().amax(dim=1, keepdim=True) / 127.0
+    ref = torch.clamp(torch.round(w / scale), -127, 127).to(torch.int8)
+    q, s = quant.quant_rows_int8(x)
+    assert n_differ > 0
+    assert np.array_equal(s, scale.squeeze(1).numpy())
+    assert np.array_equal(q, ref.numpy())
+
+
+def test_e4m3_quotient_is_rounded_to_fp32_first():
+    # As for INT8: values placed a few float32 ulps from (midpoint between two e4m3
+    # values) x scale, kept where the float32 quotient and the exact one fall on
+    # different codes; the recipe (float32 division, then torch's e4m3 cast) decides.
+    rng = np.random.default_rng(5)
+    pos = np.sort(np.unique(np.abs(quant.E4M3_VALUES[np.isfinite(quant.E4M3_VALUES)])))
+    mids = (pos[:-1] + pos[1:]) / 2.0
+    rows, n_differ = [], 0
+    while len(rows) < 8:
+        amax = np.float32(rng.uniform(1.0, 2.0))
+        s32 = np.float32(amax / np.float32(448.0))
+        vals = []
+        for m in mids:
+            base = np.float32(m * np.float64(s32))
+            for d in (-2, -1, 0, 1, 2):
+                v = base
+                for _ in range(abs(d)):
+                    v = np.nextafter(v, np.float32(np.inf if d > 0 else -np.inf), dtype=np.float32)
+                if abs(v) >= amax:
+                    continue
+                exact = np.float64(v) / np.float64(s32)
+                if quant.e4m3_encode(np.float32(v / s32)) != quant.e4m3_encode(exact):
+                    vals.append(v)
+        if vals:
+            n_differ += len(vals)
+            vals = vals[:127]
+            rows.append(np.array([amax] + vals + [0.0] * (127 - len(vals)), dtype=np.float32))
+    x = np.stack(rows)
+    w = torch.from_numpy(x)
+    scale = w.abs().amax(dim=1, keepdim=True) / 448.0
+    ref = (w / scale).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    c, s = quant.quant_rows_e4m3(x)
+    assert n_differ > 0
+    assert np.array_equal(s, scale.squeeze(1).numpy())
+    assert np.array_equal(c, ref)
+
+
 def test_e4m3_quant_bound():
     rng = np.random.default_rng(3)
     x = rng.normal(size=(16, 128)).astype(np.float32)
