@@ -1,4 +1,5 @@
-// Grouped top-k routing: one warp per token, everything in registers.
+// Grouped top-k routing: 8 lanes per token (the segmented kernel) where the shape
+// allows it, else one warp per token; everything in registers.
 //
 // Follows "GroupedTopK 算子优化入门" section 三 (score, per-group max, top
 // groups, mask, top-k, renormalise, scale) with the fusion plan of its
@@ -7,7 +8,12 @@
 // increasing, so groups and experts are selected on the logits themselves and
 // only the k selected logits are exponentiated when the weights renormalise.
 //
-// Lane l holds the logits of experts [l*VPL, (l+1)*VPL). Warp-wide maxima and
+// Segmented kernel (grouped_topk_seg_kernel): a token is L = 8 lanes of a warp,
+// lane s holding experts [s*P, (s+1)*P) after the CTA's logits are staged in
+// shared memory; its selection rounds are L-lane segment maxima plus a ballot.
+// The warp-per-token kernels below serve the shapes it does not cover.
+//
+// Warp-per-token kernels: lane l holds the logits of experts [l*VPL, (l+1)*VPL). Warp-wide maxima and
 // the lowest index among equal maxima come from redux.sync, so ties resolve to
 // the lower expert (or group) index. The fast kernel (E = 32*VPL, power-of-two
 // group count) reduces the float logits directly; the generic kernel (any E and
