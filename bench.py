@@ -407,8 +407,34 @@ def bench_decode(moe, synth, torch, dev, flush, peaks, args):
     return out
 
 
+def fp32_score_collisions(logits, scoring: str, depth: int) -> int:
+    """Rows of `logits` [T, E] in which two distinct logits among the row's `depth` largest
+    have equal float32 scores: the rows where ranking on rounded scores, instead of on the
+    logits as the kernels and the oracle do, could reorder the selection. Information only."""
+    import numpy as np
+    x = np.asarray(logits, dtype=np.float32)
+    order = np.argsort(-x, axis=1, kind="stable")[:, :depth]
+    xs = np.take_along_axis(x, order, axis=1)
+    one = np.float32(1.0)
+    if scoring == "sigmoid":
+        sc = (one / (one + np.exp(-xs))).astype(np.float32)
+    else:
+        m = x.max(axis=1, keepdims=True)
+        den = np.exp(x - m).sum(axis=1, keepdims=True, dtype=np.float32)
+        sc = (np.exp(xs - m) / den).astype(np.float32)
+    tie = (sc[:, 1:] == sc[:, :-1]) & (xs[:, 1:] != xs[:, :-1])
+    return int(tie.any(axis=1).sum())
+
+
 def bench_routing(moe, synth, torch, dev, flush, peaks, args):
     out = {}
+    for scoring in ("softmax", "sigmoid"):
+        cfg = synth.routing_config(16384, scoring)
+        g = synth.gating_logits(cfg, dev).cpu().numpy()
+        out[f"fp32_score_ties_T16384_{scoring}"] = {
+            "rows": fp32_score_collisions(g, scoring, 2 * cfg.topk), "of": 16384,
+            "note": "rows whose 16 largest logits include two distinct ones with equal float32 scores "
+                    "(selection ranks on logits; information only)"}
     for T in (16384, 65536):
         cfg = synth.routing_config(T, "sigmoid")
         g = synth.gating_logits(cfg, dev)

@@ -124,3 +124,15 @@ def test_reference_arm_prints_the_contract_line():
     assert line["cpu_baseline"]["cores"] >= 1 and "16 of 64 tokens" in line["cpu_baseline"]["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_fp32_score_collisions_counts_rows_that_rounding_would_tie():
+    import numpy as np
+    a = np.float32(20.0)
+    b = np.nextafter(a, np.float32(0.0), dtype=np.float32)   # distinct logit, same fp32 sigmoid (1.0)
+    x = np.array([[a, b, 0.0, -1.0], [3.0, 2.0, 1.0, 0.0], [0.5, 0.5, 0.0, 0.0]], dtype=np.float32)
+    assert bench.fp32_score_collisions(x, "sigmoid", 2) == 1   # equal logits are not counted
+    assert bench.fp32_score_collisions(x, "softmax", 2) == 0   # softmax keeps 20 and its neighbour apart
+    y = np.array([[0.0, -100.0, -100.00001, -200.0]], dtype=np.float32)
+    assert bench.fp32_score_collisions(y, "softmax", 3) == 1   # both underflow to 0 in float32
+    assert bench.fp32_score_collisions(y, "softmax", 2) == 0
