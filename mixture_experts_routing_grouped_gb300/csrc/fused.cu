@@ -11,10 +11,6 @@
 // on the padded length is replaced by a device-side length read by the GEMMs.
 #include "common.cuh"
 
-#include <cstdlib>
-#include <cstring>
-#include <algorithm>
-
 namespace moe {
 
 moe_status_t validate_routing(int T, int E, int G, int kg, int k, int scoring);
@@ -30,15 +26,6 @@ moe_status_t launch_gemm_gate_up_pairs(const __nv_bfloat16* x, const __nv_bfloat
                                        const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
                                        int H, int I, int E, float* y_clear, size_t y_clear_floats,
                                        int* tile_counter, cudaStream_t s);
-bool gate_up_pair2_supported(int I);
-moe_status_t launch_gemm_gate_up_pair2(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_tok,
-                                       const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk,
-                                       int H, int I, int E, cudaStream_t s);
-bool down_pair2_supported(int H, int I);
-moe_status_t launch_gemm_down_pair2(const __nv_bfloat16* h, const __nv_bfloat16* w2, const int32_t* sorted_ids,
-                                    const int32_t* sorted_tok, const int32_t* offsets, const float* topk_w,
-                                    float* y_acc, int* err, int num_pairs, int cap, int H, int I, int E,
-                                    cudaStream_t s);
 moe_status_t launch_gemm_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, const int32_t* sorted_ids,
                               const int32_t* expert_ids, const int32_t* ntpp, const float* topk_w, float* y_acc,
                               int* err, int num_pairs, int topk, int cap, int H, int I, int E, cudaStream_t s);
@@ -65,17 +52,9 @@ namespace {
 
 // Kernel choice. Decode-sized problems (at most 32 rows per expert on average)
 // use the swap-AB kernels with 16-row blocks and token tiles of <= 32; larger
-// ones use the sorted-layout kernels with 128-row blocks. The
-// MOE_GB300_PREFILL_KERNEL environment variable selects another large-problem
-// kernels for comparisons on one workload: "swap" (token tiles of <= 256 on
-// 16-row blocks) or "cta_pair" (both grouped GEMMs on CTA pairs, cta_group::2;
-// gate_up needs I a multiple of 256). The CTA-pair kernels halve what each SM
-// loads per K step but compute an expert's odd last block as a full 256-row
-// tile; at the prefill shape the one-SM kernels are slightly faster.
+// ones use the sorted-layout kernels with 128-row blocks.
 struct Plan {
   bool swap;
-  bool pair_gate_up;
-  bool pair_down;
   int nmax;
   int block_m;
 };
@@ -86,13 +65,7 @@ Plan choose_plan(int T, int E, int topk) {
   if (pairs <= 32ll * E) {
     p.swap = true; p.nmax = 32; p.block_m = 16;
   } else {
-    const char* env = std::getenv("MOE_GB300_PREFILL_KERNEL");
-    if (env && std::strcmp(env, "swap") == 0) {
-      p.swap = true; p.nmax = 256; p.block_m = 16;
-    } else {
-      p.swap = false; p.nmax = 0; p.block_m = 128;
-      p.pair_gate_up = p.pair_down = env && std::strcmp(env, "cta_pair") == 0;
-    }
+    p.swap = false; p.nmax = 0; p.block_m = 128;
   }
   return p;
 }
@@ -213,8 +186,8 @@ extern "C" void moe_set_stage_events(void* const* events, int n) {
 
 extern "C" size_t moe_fused_forward_workspace_size(int T, int H, int I, int E, int topk) {
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0) return 0;
-  // large enough for either kernel family
-  return std::max(moe::fused_layout(T, H, I, E, topk, 16).total, moe::fused_layout(T, H, I, E, topk, 128).total);
+  // the layout of the kernel family that this problem size selects
+  return moe::fused_layout(T, H, I, E, topk, moe::choose_plan(T, E, topk).block_m).total;
 }
 
 extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, const void* w_gate_up,
@@ -236,7 +209,7 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
     return MOE_ERR_UNSUPPORTED;
   const Plan plan = choose_plan(T, E, topk);
   const FusedLayout L = fused_layout(T, H, I, E, topk, plan.block_m);
-  if (!ws || ws_bytes < moe_fused_forward_workspace_size(T, H, I, E, topk) || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+  if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
 
   cudaStream_t s = as_stream(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -254,7 +227,7 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   // The fp32 accumulator of the down pass is cleared by the one-SM gate_up
   // kernel's epilogue warps while its first tiles run, else by the routing
   // kernel (each token's row).
-  const bool gate_up_clears = !plan.swap && !(plan.pair_gate_up && gate_up_pair2_supported(I));
+  const bool gate_up_clears = !plan.swap;
   stage_mark(0, s);
   st = launch_grouped_topk(gating, T, E, num_expert_group, topk_group, topk, scoring, renormalize,
                            routed_scaling_factor, topk_weights, topk_ids, s, gate_up_clears ? nullptr : y_acc, H,
@@ -269,10 +242,6 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   if (plan.swap)
     st = launch_swap_gate_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w_gate_up),
                              sorted_ids, offsets, h, err, num_pairs, topk, H, I, E, plan.nmax, s);
-  else if (plan.pair_gate_up && gate_up_pair2_supported(I))
-    st = launch_gemm_gate_up_pair2(static_cast<const __nv_bfloat16*>(x),
-                                   static_cast<const __nv_bfloat16*>(w_gate_up), sorted_tok, offsets, h, err,
-                                   num_pairs, topk, H, I, E, s);
   else
     st = launch_gemm_gate_up_pairs(static_cast<const __nv_bfloat16*>(x),
                                    static_cast<const __nv_bfloat16*>(w_gate_up), sorted_tok, offsets, h, err,
@@ -282,9 +251,6 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   if (plan.swap)
     st = launch_swap_down(h, static_cast<const __nv_bfloat16*>(w_down), sorted_ids, offsets, topk_weights, y_acc, err,
                           num_pairs, topk, L.cap, H, I, E, plan.nmax, s);
-  else if (plan.pair_down && down_pair2_supported(H, I))
-    st = launch_gemm_down_pair2(h, static_cast<const __nv_bfloat16*>(w_down), sorted_ids, sorted_tok, offsets,
-                                topk_weights, y_acc, err, num_pairs, L.cap, H, I, E, s);
   else
     st = launch_gemm_down(h, static_cast<const __nv_bfloat16*>(w_down), sorted_ids, expert_ids, ntpp, topk_weights,
                           y_acc, err, num_pairs, topk, L.cap, H, I, E, s);
