@@ -136,8 +136,11 @@ MOE_API moe_status_t moe_align_block_size(const int32_t* topk_ids, int num_pairs
  *  topk_weights [T, topk] fp32 out, topk_ids [T, topk] int32 out (the routing).
  *  ws, ws_bytes workspace of at least moe_fused_forward_workspace_size(...) bytes,
  *               256-byte aligned and zero-filled before its first use (a ticket
- *               counter inside is left at zero by every call); holds the sorted pair layout, h = silu(gate)*up in sorted order and
- *               an fp32 accumulator for y. Its first 4 bytes are the device error word.
+ *               counter inside is left at zero by every call); holds the sorted pair
+ *               layout, h = silu(gate)*up in sorted order and an fp32 accumulator for
+ *               y. Its first 4 bytes are the device error word. The size is that of
+ *               the kernels the problem size selects (16-row blocks when
+ *               T * topk <= 32 * E, else 128-row blocks).
  */
 MOE_API size_t moe_fused_forward_workspace_size(int T, int H, int I, int E, int topk);
 MOE_API moe_status_t moe_fused_forward(const void* x, const float* gating, const void* w_gate_up,
@@ -199,13 +202,18 @@ MOE_API moe_status_t moe_fused_forward_fp8(const void* x, const float* gating, c
  * allocates nothing.
  *  - Problems whose moe_fused_forward_workspace_size(T, H, I, E, topk) exceeds
  *    MOE_NOALLOC_SCRATCH_BYTES are rejected with MOE_ERR_WORKSPACE, before any launch.
+ *    The size is that of the kernels the problem selects: decode-sized problems
+ *    (T * topk <= 32 * E) use 16-row blocks, e.g. about 23 MiB at T = 128 for
+ *    E = 256, H = 7168, I = 2048, topk = 8.
  *  - The first call made while a device is current looks up the array's device
- *    address on that device (cudaGetSymbolAddress) and caches it; make that first
- *    call before any stream capture on the device.
+ *    address on that device (cudaGetSymbolAddress) and caches it with the current
+ *    CUDA context (a call under a new context, e.g. after cudaDeviceReset, looks
+ *    it up again); make that first call before any stream capture on the device.
  *  - All calls share the array, which keeps the last call's contents (nothing in
  *    it needs to start at zero). Calls whose GPU work overlaps (different streams
  *    or host threads) race on it: serialise them.
- *  - The device error word of this scratch is not exposed.
+ *  - The array's device error word collects MOE_DEVERR_* bits of every call on
+ *    the device until moe_fused_forward_noalloc_check_error reads and clears it.
  */
 #define MOE_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 MOE_API moe_status_t moe_fused_forward_noalloc(const void* x, const float* gating,
@@ -215,6 +223,15 @@ MOE_API moe_status_t moe_fused_forward_noalloc(const void* x, const float* gatin
                                                int renormalize, float routed_scaling_factor,
                                                void* y, float* topk_weights, int32_t* topk_ids,
                                                void* stream);
+
+/*
+ * moe_fused_forward_noalloc_check_error -- moe_check_device_error for the scratch
+ * array of moe_fused_forward_noalloc on the current device: synchronises `stream`,
+ * writes the MOE_DEVERR_* bits collected since the last check to *code and clears
+ * them. Allocates nothing. Returns MOE_OK if no bit was set, MOE_ERR_DEVICE_DATA
+ * otherwise.
+ */
+MOE_API moe_status_t moe_fused_forward_noalloc_check_error(int* code, void* stream);
 
 /*
  * moe_set_stage_events -- optional per-stage timing of moe_fused_forward (not in the

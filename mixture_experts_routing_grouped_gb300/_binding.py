@@ -35,6 +35,7 @@ _SIGNATURES = {
                                        _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "moe_fused_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                            _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp]),
+    "moe_fused_forward_noalloc_check_error": (_c_int, [ctypes.POINTER(_c_int), _vp]),
     "moe_quant_per_token": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "gmm_lowp_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "gmm_lowp": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
@@ -253,6 +254,19 @@ def moe_fused_forward_noalloc(x: torch.Tensor, gating: torch.Tensor, w_gate_up: 
                                          _ptr(topk_weights), _ptr(topk_ids), _stream(x))
     _check("moe_fused_forward_noalloc", st)
     return y, topk_weights, topk_ids
+
+
+def moe_fused_forward_noalloc_check_error(device: torch.device | None = None) -> int:
+    """Reads and clears the device error word of moe_fused_forward_noalloc's scratch array on
+    the current device (synchronises the current stream); returns the MOE_DEVERR_* bits."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    code = _c_int(0)
+    with torch.cuda.device(dev):
+        st = lib().moe_fused_forward_noalloc_check_error(ctypes.byref(code),
+                                                         ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+    if st not in (MOE_OK, MOE_ERR_DEVICE_DATA):
+        _check("moe_fused_forward_noalloc_check_error", st)
+    return int(code.value)
 
 
 # --------------------------------------------------------------------------- low precision

@@ -5,7 +5,8 @@ array inside the library instead of a caller workspace.
 
 Checked through the C ABI against moe_fused_forward on the same inputs, on two
 calls in a row (the shared array keeps the previous call's contents), plus the
-rejection of a problem too large for the array. This file is collected last so
+rejection of a problem too large for the array, and the read-and-clear of the
+array's device error word. This file is collected last so
 that a run stopping at the first failure has already run every other test."""
 import ctypes
 
@@ -28,6 +29,11 @@ CONFIGS = [
     synth.MoEConfig("ragged_T1000_H768_I384_E16_top4_grouped", T=1000, H=768, I=384, E=16, topk=4,
                     num_expert_group=4, topk_group=2, scoring="sigmoid", routed_scaling_factor=2.5,
                     logit_sigma=2.0, seed=11),
+    # decode-shaped: 256 experts, grouped sigmoid top-8, T * topk <= 32 * E selects the 16-row-block kernels,
+    # whose scratch is far below that of the 128-row layout
+    synth.MoEConfig("decode_like_T32_H1024_I512_E256_top8", T=32, H=1024, I=512, E=256, topk=8,
+                    num_expert_group=8, topk_group=4, scoring="sigmoid", routed_scaling_factor=2.5,
+                    logit_sigma=2.0, seed=15),
 ]
 
 
@@ -46,6 +52,8 @@ def test_noalloc_matches_workspace_entry_point(cfg):
         assert torch.equal(ids, ref_ids)
         assert_weights_close(w.cpu().numpy(), ref_w.cpu().numpy())
         assert_moe_close(y.float().cpu().numpy(), ref_y.float().cpu().numpy())
+    # nothing went wrong on the device, and reading the scratch's error word clears it
+    assert moe.moe_fused_forward_noalloc_check_error() == 0
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
@@ -57,3 +65,12 @@ def test_noalloc_rejects_problems_beyond_the_scratch():
     fake = ctypes.c_void_p(0x10000)   # rejected on the host before any pointer is used
     st = L.moe_fused_forward_noalloc(fake, fake, fake, fake, T, H, I, E, 1, 1, k, 0, 1, 1.0, fake, fake, fake, None)
     assert st == 3   # MOE_ERR_WORKSPACE
+
+
+def test_noalloc_accepts_the_decode_workload_sizes():
+    """The decode workload (E=256, H=7168, I=2048, top-8) runs the 16-row-block kernels at
+    T <= 128, whose scratch fits the array; the size check follows the selected kernels."""
+    import mixture_experts_routing_grouped_gb300 as moe
+    limit = 64 * 1024 * 1024
+    for T in (1, 8, 32, 128):
+        assert 0 < moe.moe_fused_forward_workspace_size(T, 7168, 2048, 256, 8) <= limit
