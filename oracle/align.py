@@ -1,9 +1,10 @@
 """``moe_align_block_size`` plainly (test infrastructure; see ``oracle/__init__``).
 
-Follows the mini-sglang MoE chapter ("fused MoE", ``moe_align_block_size``):
-stably sort the flat (token, expert) pair indices by expert, pad every
-expert's segment to a multiple of ``block_m`` with the sentinel ``num_pairs``,
-and give every block of ``block_m`` entries its expert.
+Follows the mini-sglang MoE chapter ("fused MoE", ``moe_align_block_size``),
+whose result is fixed by its description: the flat (token, expert) pair indices
+stably sorted by expert, every expert's segment padded to a multiple of
+``block_m`` with the sentinel ``num_pairs``, and every block of ``block_m``
+entries labelled with its expert.
 
 Reading of the output buffers (the page returns exactly-sized tensors): the
 buffers here have the fixed capacity ``max_padded(num_pairs, E, block_m)`` so
@@ -24,23 +25,44 @@ def max_padded(num_pairs: int, E: int, block_m: int) -> int:
 
 
 def moe_align_block_size(topk_ids: np.ndarray, block_m: int, num_experts: int):
-    """Returns (sorted_token_ids, expert_ids, expert_offsets, num_tokens_post_padded)."""
-    flat = np.asarray(topk_ids).reshape(-1).astype(np.int64)
-    num_pairs = flat.size
+    """Returns (sorted_token_ids, expert_ids, expert_offsets, num_tokens_post_padded).
+
+    Written as a counting sort with one write cursor per expert:
+
+    1. count the pairs that chose each expert;
+    2. lay the experts' segments out back to back, each segment its count rounded
+       up to a multiple of ``block_m``;
+    3. visit the pairs in increasing pair index and write each into the next free
+       slot of its expert's segment (visiting in index order is what makes the
+       sort stable);
+    4. every block of ``block_m`` slots gets the expert whose segment holds it.
+    """
+    pair_expert = [int(e) for e in np.asarray(topk_ids).reshape(-1)]
+    num_pairs = len(pair_expert)
     E = num_experts
-    counts = np.bincount(flat, minlength=E)                       # pairs per expert
-    padded = (counts + block_m - 1) // block_m * block_m          # segment length
-    seg_start = np.cumsum(padded) - padded                        # exclusive prefix sum
-    order = np.argsort(flat, kind="stable")                       # pairs ordered by expert
-    sorted_expert = flat[order]
-    first_of_expert = np.cumsum(counts) - counts
-    rank = np.arange(num_pairs) - first_of_expert[sorted_expert]  # rank within its expert
-    total = int(padded.sum())
+
+    count = [0] * E                                               # 1.
+    for e in pair_expert:
+        count[e] += 1
+
+    seg_begin, seg_len, pos = [], [], 0                           # 2.
+    for e in range(E):
+        length = -(-count[e] // block_m) * block_m
+        seg_begin.append(pos)
+        seg_len.append(length)
+        pos += length
+    total = pos
 
     cap = max_padded(num_pairs, E, block_m)
-    sorted_ids = np.full(cap, num_pairs, dtype=np.int32)
-    sorted_ids[seg_start[sorted_expert] + rank] = order.astype(np.int32)
-    expert_ids = np.full(cap // block_m, -1, dtype=np.int32)
-    expert_ids[:total // block_m] = np.repeat(np.arange(E), padded // block_m)
-    expert_offsets = np.concatenate([seg_start, [total]]).astype(np.int32)
+    sorted_ids = np.full(cap, num_pairs, dtype=np.int32)          # padding holds the sentinel
+    cursor = list(seg_begin)                                      # 3.
+    for p, e in enumerate(pair_expert):
+        sorted_ids[cursor[e]] = p
+        cursor[e] += 1
+
+    expert_ids = np.full(cap // block_m, -1, dtype=np.int32)      # 4.
+    for e in range(E):
+        first_block = seg_begin[e] // block_m
+        expert_ids[first_block:first_block + seg_len[e] // block_m] = e
+    expert_offsets = np.array(seg_begin + [total], dtype=np.int32)
     return sorted_ids, expert_ids, expert_offsets, total

@@ -3,10 +3,10 @@
 Two independent formulations of the same sum, both in float64 with no
 intermediate rounding:
 
-* ``expert_loop_forward`` -- the "expert view" of the mini-sglang MoE chapter
-  (``TorchMoeBackend.forward``): for every selected expert, gather its tokens,
-  run the SwiGLU MLP, scale by the route weight and add back into the tokens'
-  rows;
+* ``expert_loop_forward`` -- the "expert view" that the mini-sglang MoE chapter
+  contrasts with the token view: the (token, slot) pairs are grouped by the
+  expert they chose, each expert's SwiGLU MLP runs once over its pairs' tokens,
+  and every pair's weighted result is added into its token's row;
 * ``token_view_forward`` -- the "token view" of "Fused MoE Part 3" (section
   01, ``selected_weights = weight[topk_ids]``): every token is projected by the
   weights of its own selected experts, one (token, slot) pair at a time.
@@ -45,27 +45,37 @@ def expert_projection(x: np.ndarray, weight: np.ndarray, topk_ids: np.ndarray) -
     return out
 
 
+def _expert_matrix(w, e: int) -> np.ndarray:
+    """Expert e's matrix from an [E, ...] array, or from a callable e -> matrix (so that the
+    experts of a large layer can be fetched and converted one at a time)."""
+    return np.asarray(w(e) if callable(w) else w[e], dtype=np.float64)
+
+
 def expert_loop_forward(x, w1, w2, topk_weights, topk_ids) -> np.ndarray:
-    """Expert view (mini-sglang TorchMoeBackend): y [T, H] float64."""
+    """The layer summed one expert at a time (the chapter's expert view): y [T, H] float64.
+
+    y[t] = sum over slots j of w[t, j] * W2_e (silu(G_e x_t) * U_e x_t), e = ids[t, j].
+    The (token, slot) pairs are grouped by the expert they chose, so that each
+    expert's matrices are read once for all of its pairs; each pair's contribution
+    is then added into its token's row. ``w1`` [E, 2I, H] (gate rows [0, I), up rows
+    [I, 2I)) and ``w2`` [E, H, I] are arrays or callables e -> that expert's matrix.
+    """
     x = np.asarray(x, dtype=np.float64)
-    w1 = np.asarray(w1, dtype=np.float64)
-    w2 = np.asarray(w2, dtype=np.float64)
-    I = w1.shape[1] // 2
-    T, topk = np.asarray(topk_ids).shape
-    flat_ids = np.asarray(topk_ids).reshape(-1)
-    flat_w = np.asarray(topk_weights, dtype=np.float64).reshape(-1)
-    token_of_pair = np.repeat(np.arange(T), topk)
-    out = np.zeros_like(x)
-    for e in np.unique(flat_ids):
-        sel = np.nonzero(flat_ids == e)[0]
-        tokens = token_of_pair[sel]
-        xs = x[tokens]
-        gate = xs @ w1[e, :I].T
-        up = xs @ w1[e, I:].T
-        h = silu(gate) * up
-        y = (h @ w2[e].T) * flat_w[sel][:, None]
-        np.add.at(out, tokens, y)
-    return out
+    ids = np.asarray(topk_ids)
+    tw = np.asarray(topk_weights, dtype=np.float64)
+    y = np.zeros_like(x)
+    for e in sorted(set(ids.reshape(-1).tolist())):
+        pair_tok, pair_slot = np.nonzero(ids == e)      # the pairs routed to e, token by token
+        W1e = _expert_matrix(w1, e)
+        I = W1e.shape[0] // 2
+        xs = x[pair_tok]
+        gate_proj = xs @ W1e[:I].T
+        up_proj = xs @ W1e[I:].T
+        act = silu(gate_proj) * up_proj                 # [pairs of e, I]
+        contrib = (act @ _expert_matrix(w2, e).T) * tw[pair_tok, pair_slot][:, None]
+        for r, t in enumerate(pair_tok):
+            y[t] += contrib[r]
+    return y
 
 
 def token_view_forward(x, w1, w2, topk_weights, topk_ids) -> np.ndarray:
@@ -176,3 +186,41 @@ def token_outputs_fp8(x_row, qw1_experts, sw1_experts, qw2_experts, sw2_experts,
         qh, sh = quant.quant_rows_e4m3(h[None, :])
         out = out + float(wj) * (w2 @ (quant.dequant(qh[0], "e4m3") * float(sh[0])))
     return out
+
+
+def expert_loop_forward_fp8(x, qw1, sw1, qw2, sw2, topk_weights, topk_ids) -> np.ndarray:
+    """Steps 2-5 of ``fused_forward_fp8`` summed one expert at a time: y float64 [T, H].
+
+    The same arithmetic as the token loop (``token_outputs_fp8``), grouped by expert
+    so that each expert's codes are decoded once for all of its (token, slot) pairs:
+    x is quantised per token; for expert e and each of its pairs, g and u are the
+    scaled products of the decoded codes, h = silu(g) * u is held in bfloat16 and
+    quantised per pair row, and the down product scaled by both scales and the route
+    weight is added into the pair's token row. ``qw1`` / ``sw1`` / ``qw2`` / ``sw2``
+    are arrays indexed by expert ([E, 2I, H], [E, 2I], [E, H, I], [E, H]) or callables
+    e -> that expert's slice.
+    """
+    from . import quant
+    x = np.asarray(x, dtype=np.float32)
+    ids = np.asarray(topk_ids)
+    tw = np.asarray(topk_weights, dtype=np.float64)
+    qx, sx = quant.quant_rows_e4m3(x)                                       # one scale per token
+    dx = quant.dequant(qx, "e4m3") * sx.astype(np.float64)[:, None]
+    y = np.zeros((x.shape[0], x.shape[1]))
+
+    def part(w, e):
+        return np.asarray(w(e) if callable(w) else w[e])
+
+    for e in sorted(set(ids.reshape(-1).tolist())):
+        pair_tok, pair_slot = np.nonzero(ids == e)
+        w1 = quant.dequant(part(qw1, e), "e4m3") * part(sw1, e).astype(np.float64)[:, None]
+        I = w1.shape[0] // 2
+        xs = dx[pair_tok]
+        hs = _bf16_round(silu(xs @ w1[:I].T) * (xs @ w1[I:].T))            # held in bfloat16
+        qh, sh = quant.quant_rows_e4m3(hs)                                  # one scale per pair row
+        w2 = quant.dequant(part(qw2, e), "e4m3") * part(sw2, e).astype(np.float64)[:, None]
+        dh = quant.dequant(qh, "e4m3") * sh.astype(np.float64)[:, None]
+        contrib = (dh @ w2.T) * tw[pair_tok, pair_slot][:, None]
+        for r, t in enumerate(pair_tok):
+            y[t] += contrib[r]
+    return y

@@ -31,14 +31,18 @@ def test_end_to_end_example_from_logits():
 
 
 def _brute(flat, E, bm):
-    buckets = [[] for _ in range(E)]
-    for p, e in enumerate(flat):           # pairs visited in order: stable by construction
-        buckets[e].append(p)
-    out, blocks = [], []
+    # Python's sort is stable: sorting the pair indices by their expert keeps equal
+    # experts in pair order. Then cut the sorted list into per-expert runs and pad each.
+    order = sorted(range(len(flat)), key=lambda p: flat[p])
+    out, blocks, i = [], [], 0
     for e in range(E):
-        seg = buckets[e] + [len(flat)] * ((-len(buckets[e])) % bm)
+        j = i
+        while j < len(order) and flat[order[j]] == e:
+            j += 1
+        seg = order[i:j] + [len(flat)] * ((-(j - i)) % bm)
         out += seg
         blocks += [e] * (len(seg) // bm)
+        i = j
     return out, blocks
 
 

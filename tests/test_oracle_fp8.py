@@ -130,3 +130,22 @@ def test_e4m3_zero_row_gets_scale_one():
     c, s = quant.quant_rows_e4m3(x)
     assert s[0] == 1.0 and np.all(c[0] == 0)
     assert s[1] == np.float32(3.0) / np.float32(448.0) and c[1, 5] == 0x80 | E4M3_448
+
+
+def test_fp8_expert_loop_equals_token_loop():
+    # The expert-grouped form (used for layers too large for the token loop) sums the
+    # same per-pair terms: it equals the token loop to float64 rounding on random layers,
+    # with ties and repeats of experts across tokens.
+    rng = np.random.default_rng(21)
+    for T, H, I, E, k in ((9, 32, 16, 5, 2), (17, 64, 32, 8, 3)):
+        x = rng.normal(size=(T, H)).astype(np.float32)
+        q1, s1 = quant.quant_rows_e4m3(rng.normal(0, 0.1, size=(E * 2 * I, H)))
+        q2, s2 = quant.quant_rows_e4m3(rng.normal(0, 0.1, size=(E * H, I)))
+        gating = rng.normal(size=(T, E)).astype(np.float32)
+        args = (q1.reshape(E, 2 * I, H), s1.reshape(E, 2 * I), q2.reshape(E, H, I), s2.reshape(E, H))
+        y, tw, ids = moe.fused_forward_fp8(x, gating, *args, k, True)
+        y2 = moe.expert_loop_forward_fp8(x, *args, tw, ids)
+        np.testing.assert_allclose(y2, y, rtol=1e-12, atol=1e-12)
+        # per-expert callables give the same sum as the arrays
+        y3 = moe.expert_loop_forward_fp8(x, *(lambda e, a=a: a[e] for a in args), tw, ids)
+        assert np.array_equal(y3, y2)

@@ -38,17 +38,21 @@ MISTAKES = [
     # align (mini-sglang moe_align_block_size)
     ("align.py", "sorted_ids = np.full(cap, num_pairs, dtype=np.int32)",
      "sorted_ids = np.full(cap, num_pairs - 1, dtype=np.int32)", "sentinel off by one"),
-    ("align.py", "padded = (counts + block_m - 1) // block_m * block_m", "padded = (counts + block_m) // block_m * block_m",
+    ("align.py", "length = -(-count[e] // block_m) * block_m", "length = (count[e] // block_m + 1) * block_m",
      "over-padding"),
-    ("align.py", 'order = np.argsort(flat, kind="stable")',
-     'order = (num_pairs - 1 - np.argsort(flat[::-1], kind="stable"))', "unstable within an expert"),
+    ("align.py", "    for p, e in enumerate(pair_expert):\n        sorted_ids",
+     "    for p, e in reversed(list(enumerate(pair_expert))):\n        sorted_ids", "unstable within an expert"),
     ("align.py", "expert_ids = np.full(cap // block_m, -1, dtype=np.int32)",
      "expert_ids = np.full(cap // block_m, 0, dtype=np.int32)", "trailing block experts 0"),
-    ("align.py", "expert_offsets = np.concatenate([seg_start, [total]]).astype(np.int32)",
-     "expert_offsets = np.concatenate([seg_start, [num_pairs]]).astype(np.int32)", "offsets end at the pair count"),
+    ("align.py", "expert_offsets = np.array(seg_begin + [total], dtype=np.int32)",
+     "expert_offsets = np.array(seg_begin + [num_pairs], dtype=np.int32)", "offsets end at the pair count"),
     # MoE forward (mini-sglang TorchMoeBackend; Fused MoE Part 3)
-    ("moe.py", "        h = silu(gate) * up", "        h = silu(up) * gate", "gate and up swapped (expert loop)"),
-    ("moe.py", "        y = (h @ w2[e].T) * flat_w[sel][:, None]", "        y = (h @ w2[e].T)", "route weight dropped"),
+    ("moe.py", "        act = silu(gate_proj) * up_proj", "        act = silu(up_proj) * gate_proj",
+     "gate and up swapped (expert loop)"),
+    ("moe.py", "        contrib = (act @ _expert_matrix(w2, e).T) * tw[pair_tok, pair_slot][:, None]",
+     "        contrib = act @ _expert_matrix(w2, e).T", "route weight dropped"),
+    ("moe.py", "        contrib = (act @ _expert_matrix(w2, e).T) * tw[pair_tok, pair_slot][:, None]",
+     "        contrib = (act @ _expert_matrix(w2, e).T) * tw[pair_tok, 0][:, None]", "route weight of slot 0"),
     ("moe.py", "    return v / (1.0 + np.exp(-v))", "    return np.maximum(v, 0.0)", "relu instead of silu"),
     ("moe.py", "    h = silu(gu[:, :, :I]) * gu[:, :, I:]", "    h = silu(gu[:, :, I:]) * gu[:, :, :I]",
      "gate and up swapped (token view)"),
@@ -64,6 +68,12 @@ MISTAKES = [
      "        out = out + float(wj) * (w2 @ h)", "FP8 layer: h not quantised"),
     ("moe.py", "        h = _bf16_round(silu(w1[:I] @ dx) * (w1[I:] @ dx))",
      "        h = _bf16_round(silu(w1[I:] @ dx) * (w1[:I] @ dx))", "FP8 layer: gate and up swapped"),
+    ("moe.py", "        hs = _bf16_round(silu(xs @ w1[:I].T) * (xs @ w1[I:].T))",
+     "        hs = silu(xs @ w1[:I].T) * (xs @ w1[I:].T)", "FP8 expert loop: h not held in bf16"),
+    ("moe.py", '    dx = quant.dequant(qx, "e4m3") * sx.astype(np.float64)[:, None]',
+     '    dx = quant.dequant(qx, "e4m3")', "FP8 expert loop: token scale dropped"),
+    ("moe.py", "        contrib = (dh @ w2.T) * tw[pair_tok, pair_slot][:, None]",
+     "        contrib = (hs @ w2.T) * tw[pair_tok, pair_slot][:, None]", "FP8 expert loop: h not quantised"),
     # quantisers and the E4M3 code book (low-precision GMM article; OCP FP8)
     ("quant.py", "INT8_QMAX = 127.0", "INT8_QMAX = 128.0", "INT8 range 128"),
     ("quant.py", "q = np.clip(np.rint(quot), -INT8_QMAX, INT8_QMAX)",
