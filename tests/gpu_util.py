@@ -18,13 +18,18 @@ def assert_weights_close(got, ref, rel=1e-6):
     assert not bad.any(), f"{bad.sum()} weights off by more than {rel} relative; worst {np.abs(got-ref).max()}"
 
 
-def assert_moe_close(got, ref):
-    """bf16 layer output vs the float64 oracle: |d| <= 2e-2 * max(1, |ref|) per element,
-    and relative Frobenius error <= 1e-2."""
+def assert_moe_close(got, ref, rel_above_one=False):
+    """bf16 layer output vs the float64 oracle: max |d| <= 2e-2 per element and relative
+    Frobenius error <= 1e-2.
+
+    ``rel_above_one`` widens the per-element bound to 2e-2 * max(1, |ref|): for layers
+    whose outputs reach |y| >= 8 (the decode workload, scaled by 2.5), where one bf16
+    rounding of y alone can move it by half an ulp = 2^-5 > 2e-2.
+    """
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     d = np.abs(got - ref)
-    bound = 2e-2 * np.maximum(1.0, np.abs(ref))
+    bound = 2e-2 * (np.maximum(1.0, np.abs(ref)) if rel_above_one else 1.0)
     assert (d <= bound).all(), f"max |dy| = {d.max():.3e} at {np.unravel_index(d.argmax(), d.shape)}"
     nref = np.linalg.norm(ref)
     if nref > 0:

@@ -1,9 +1,9 @@
 """GPU moe_fused_forward (routing -> align -> gate_up GEMM + SwiGLU -> down GEMM
 + weighted combine) vs the float64 oracle.
 
-Small layers are compared element by element on the whole output; the full
-prefill and decode workloads on sampled tokens (each sampled token's output is
-recomputed by the oracle from its own experts), plus exact routing on all tokens.
+Every test compares the whole output element by element: small layers against the
+oracle's whole-layer function, the full prefill and decode workloads against its
+expert loop fed one expert's weights at a time; routing ids bit-exact on all tokens.
 """
 import numpy as np
 import pytest
@@ -69,37 +69,42 @@ def test_small_layers(cfg):
     _full_check(cfg)
 
 
-def _sampled_check(cfg, n_samples=12):
+def _host_f64(t):
+    """One expert's bf16 matrix as float64 on the host (the exact conversion happens on the device)."""
+    return t.double().cpu().numpy()
+
+
+def _workload_check(cfg, rel_above_one=False):
+    """The whole output of a full-size workload against the oracle's expert loop, every element.
+
+    The oracle fetches each active expert's weights from the device copy (made by the seeded
+    generator, never by the library) one expert at a time, so the layer never has to be held
+    in float64 on the host at once."""
     import mixture_experts_routing_grouped_gb300 as moe
     acts = synth.moe_activations(cfg, "cuda")
     W = synth.moe_weights(cfg, "cuda")
     ws = torch.zeros(moe.moe_fused_forward_workspace_size(cfg.T, cfg.H, cfg.I, cfg.E, cfg.topk),
                      dtype=torch.uint8, device="cuda")
     y, tw, ids = _fused(cfg, acts, W, ws)
+    assert moe.moe_check_device_error(ws) == 0
     g = acts["gating"].cpu().numpy()
     rw, rids = routing.grouped_topk(g, cfg.topk, cfg.renormalize, cfg.num_expert_group, cfg.topk_group,
                                     cfg.scoring, cfg.routed_scaling_factor)
     assert np.array_equal(ids.cpu().numpy(), rids)
     assert_weights_close(tw.cpu().numpy(), rw)
-    rng = np.random.default_rng(cfg.T)
-    toks = sorted(set([0, cfg.T - 1] + rng.integers(0, cfg.T, size=n_samples).tolist()))
-    x = acts["x"].float().cpu().numpy()
-    got = y[toks].float().cpu().numpy()
-    ref = np.stack([omoe.token_outputs(x[t], [W["w1"][e].float().cpu().numpy() for e in rids[t]],
-                                       [W["w2"][e].float().cpu().numpy() for e in rids[t]], rw[t]) for t in toks])
-    assert_moe_close(got, ref)
-    assert moe.moe_check_device_error(ws) == 0
-    yf = y.float()
-    assert torch.isfinite(yf).all()
+    x = acts["x"].double().cpu().numpy()
+    ry = omoe.expert_loop_forward(x, lambda e: _host_f64(W["w1"][e]), lambda e: _host_f64(W["w2"][e]), rw, rids)
+    assert_moe_close(y.float().cpu().numpy(), ry, rel_above_one=rel_above_one)
 
 
-def test_prefill_workload_sampled():
-    _sampled_check(synth.prefill_config())
+def test_prefill_workload_whole():
+    _workload_check(synth.prefill_config())
 
 
 @pytest.mark.parametrize("T", [1, 8, 32, 128])
-def test_decode_workload_sampled(T):
-    _sampled_check(synth.decode_config(T), n_samples=6)
+def test_decode_workload_whole(T):
+    # outputs scaled by 2.5 reach |y| >= 8, where one bf16 rounding exceeds 2e-2 absolute
+    _workload_check(synth.decode_config(T), rel_above_one=True)
 
 
 def test_T0_is_a_no_op():
