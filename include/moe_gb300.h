@@ -86,6 +86,34 @@ MOE_API moe_status_t moe_grouped_topk(const float* gating, int T, int E, int num
                               int32_t* topk_ids, void* stream);
 
 /*
+ * moe_router_topk -- the router projection, then grouped top-k routing.
+ * Defined by the mini-sglang MoE chapter, MoEMLP.forward (gate = a replicated linear
+ * layer H -> E whose output, the router logits, feeds select_experts) and by
+ * "GroupedTopK 算子优化入门" section 二, whose gating_output is that output; the
+ * routing step is moe_grouped_topk's.
+ *
+ *  x              [T, H] bf16 hidden states.
+ *  w_gate         [E, H] fp32 router weights (K-major, as a linear layer's weight).
+ *  T, H, E        tokens (>= 0), hidden size (multiple of 32), experts (1..MOE_MAX_EXPERTS).
+ *  num_expert_group, topk_group, topk, scoring, renormalize, routed_scaling_factor:
+ *                 as for moe_grouped_topk.
+ *  router_logits  [T, E] fp32 out: sum_k x[t,k] * w_gate[e,k], every product and sum an
+ *                 fp32 operation in a fixed order (the same bits on every call); within
+ *                 H * 2^-24 * sum_k |x[t,k] w_gate[e,k]| of the exact value.
+ *  topk_weights   [T, topk] fp32 out, topk_ids [T, topk] int32 out: grouped top-k of
+ *                 router_logits (selection on those fp32 logits).
+ *  ws, ws_bytes   at least moe_router_topk_workspace_size(T, H, E) bytes, 256-byte
+ *                 aligned (partial sums when few tokens split H across CTAs); may be
+ *                 NULL when that size is 0. Nothing in it needs to start at zero.
+ */
+MOE_API size_t moe_router_topk_workspace_size(int T, int H, int E);
+MOE_API moe_status_t moe_router_topk(const void* x, const float* w_gate, int T, int H, int E,
+                                     int num_expert_group, int topk_group, int topk, int scoring,
+                                     int renormalize, float routed_scaling_factor, float* router_logits,
+                                     float* topk_weights, int32_t* topk_ids, void* ws, size_t ws_bytes,
+                                     void* stream);
+
+/*
  * moe_align_block_size -- sort the (token, expert) pairs by expert and pad.
  * Defined by the mini-sglang MoE chapter, "fused MoE", moe_align_block_size: a
  * stable sort of the flat pair indices p = token*topk + slot by expert id, every

@@ -24,6 +24,9 @@ _c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, 
 
 _SIGNATURES = {
     "moe_grouped_topk": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp]),
+    "moe_router_topk_workspace_size": (_c_size, [_c_int, _c_int, _c_int]),
+    "moe_router_topk": (_c_int, [_vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                 _vp, _vp, _vp, _vp, _c_size, _vp]),
     "moe_align_max_padded": (_c_size, [_c_int, _c_int, _c_int]),
     "moe_align_workspace_size": (_c_size, [_c_int, _c_int, _c_int]),
     "moe_align_block_size": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
@@ -118,6 +121,42 @@ def moe_grouped_topk(gating: torch.Tensor, topk: int, renormalize: bool = True, 
                                 _ptr(topk_ids), _stream(gating))
     _check("moe_grouped_topk", st)
     return topk_weights, topk_ids
+
+
+def moe_router_topk_workspace_size(T: int, H: int, E: int) -> int:
+    return int(lib().moe_router_topk_workspace_size(T, H, E))
+
+
+def moe_router_topk(x: torch.Tensor, w_gate: torch.Tensor, topk: int, renormalize: bool = True,
+                    num_expert_group: int = 1, topk_group: int = 1, scoring_func: str = "softmax",
+                    routed_scaling_factor: float = 1.0, router_logits: torch.Tensor | None = None,
+                    topk_weights: torch.Tensor | None = None, topk_ids: torch.Tensor | None = None,
+                    ws: torch.Tensor | None = None):
+    """Router projection x [T, H] bf16 @ w_gate [E, H] fp32 ^T, then grouped top-k
+    -> (router_logits fp32 [T, E], topk_weights fp32 [T, topk], topk_ids int32 [T, topk])."""
+    _need(x, "x", torch.bfloat16)
+    T, H = x.shape
+    E = w_gate.shape[0]
+    _need(w_gate, "w_gate", torch.float32, (E, H))
+    dev = x.device
+    if router_logits is None:
+        router_logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty((T, topk), dtype=torch.float32, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    _need(router_logits, "router_logits", torch.float32, (T, E))
+    _need(topk_weights, "topk_weights", torch.float32, (T, topk))
+    _need(topk_ids, "topk_ids", torch.int32, (T, topk))
+    wsb = moe_router_topk_workspace_size(T, H, E)
+    if ws is None and wsb > 0:
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    st = lib().moe_router_topk(_ptr(x), _ptr(w_gate), T, H, E, num_expert_group, topk_group, topk,
+                               SCORING[scoring_func], int(bool(renormalize)), float(routed_scaling_factor),
+                               _ptr(router_logits), _ptr(topk_weights), _ptr(topk_ids), _ptr(ws),
+                               0 if ws is None else ws.numel(), _stream(x))
+    _check("moe_router_topk", st)
+    return router_logits, topk_weights, topk_ids
 
 
 # --------------------------------------------------------------------------- align

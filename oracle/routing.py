@@ -19,6 +19,12 @@ Readings where the pages leave a step open:
   renormalised (3.6 lists it after the renormalisation without a condition).
 * Output order is the ranking order (descending weight, ties by index).
 * Inputs are finite; NaN and infinities are outside the contract.
+* Router logits (``router_logits``): the mini-sglang chapter's ``MoEMLP`` computes
+  them with ``gate = LinearReplicated(H, E)``, i.e. ``x @ W_g^T``; the blog's
+  ``gating_output`` is that output. The pages give no precision for it; the
+  reading here is the dot product of the bfloat16 hidden state and the float32
+  router weights accumulated in float64 and rounded once to float32 (the
+  routing's input dtype).
 """
 from __future__ import annotations
 
@@ -90,3 +96,26 @@ def select_experts(gating_output: np.ndarray, topk: int, renormalize: bool):
     """
     return grouped_topk(gating_output, topk, renormalize, num_expert_group=1, topk_group=1,
                         scoring_func="softmax", routed_scaling_factor=1.0)
+
+
+def router_logits(hidden_states: np.ndarray, w_gate: np.ndarray) -> np.ndarray:
+    """Router projection ``x @ W_g^T`` (mini-sglang MoE chapter, ``MoEMLP.gate``).
+
+    ``hidden_states`` [T, H] (bfloat16 values, exact in float64), ``w_gate`` [E, H]
+    float32 -> logits float32 [T, E], summed in float64 and rounded once.
+    """
+    x = np.asarray(hidden_states, dtype=np.float64)
+    w = np.asarray(w_gate, dtype=np.float64)
+    if x.ndim != 2 or w.ndim != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError("hidden_states [T, H] and w_gate [E, H] must share H")
+    return (x @ w.T).astype(np.float32)
+
+
+def router_topk(hidden_states: np.ndarray, w_gate: np.ndarray, topk: int, renormalize: bool,
+                num_expert_group: int = 1, topk_group: int = 1, scoring_func: str = "softmax",
+                routed_scaling_factor: float = 1.0):
+    """The router followed by grouped top-k: (logits float32 [T, E], topk_weights, topk_ids)."""
+    logits = router_logits(hidden_states, w_gate)
+    w, ids = grouped_topk(logits, topk, renormalize, num_expert_group, topk_group, scoring_func,
+                          routed_scaling_factor)
+    return logits, w, ids

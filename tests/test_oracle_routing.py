@@ -160,3 +160,45 @@ def test_hidden_states_not_an_input():
     # the oracle's interface has no hidden_states argument at all.
     import inspect
     assert "hidden_states" not in inspect.signature(routing.grouped_topk).parameters
+
+
+# --------------------------------------------------------------------------- router projection
+def test_router_hand_worked_example():
+    # Two tokens, H = 4, E = 3 (non-square, so a transposed operand cannot pass), values
+    # chosen so that every product and sum is exact:
+    #   token 0: e0 = 1*1 = 1; e1 = 2*0.25 + (-1)*1 = -0.5; e2 = 1*2 + 2*(-1) + 0*0.5 = 0
+    #   token 1: e0 = 0.5;     e1 = 4*1 = 4;                e2 = 0.5*2 = 1
+    x = np.array([[1.0, 2.0, 0.0, -1.0], [0.5, 0.0, 0.0, 4.0]])
+    wg = np.array([[1.0, 0.0, 0.0, 0.0], [0.0, 0.25, 0.0, 1.0], [2.0, -1.0, 0.5, 0.0]], dtype=np.float32)
+    logits = routing.router_logits(x, wg)
+    assert logits.dtype == np.float32
+    assert logits.tolist() == [[1.0, -0.5, 0.0], [0.5, 4.0, 1.0]]
+    _, w, ids = routing.router_topk(x, wg, 2, True)
+    assert ids.tolist() == [[0, 2], [1, 2]]
+    # renormalised softmax of two logits a > b: 1 / (1 + e^(b - a)) and the rest
+    e = np.e
+    np.testing.assert_allclose(w, [[e / (e + 1), 1 / (e + 1)], [1 / (1 + e ** -3), e ** -3 / (1 + e ** -3)]],
+                               rtol=1e-7)
+
+
+def test_router_logits_exact_sum_rounded_once():
+    # Against the exact rational dot product (fractions): float64 accumulation then one
+    # rounding to float32 lands within one float32 ulp of the exact value.
+    from fractions import Fraction
+    rng = np.random.default_rng(17)
+    T, H, E = 5, 96, 7
+    x = rng.normal(size=(T, H)).astype(np.float32).astype(np.float64)
+    x = np.round(x * 256) / 256                                  # bfloat16-like short values
+    wg = rng.normal(0, 0.05, size=(E, H)).astype(np.float32)
+    logits = routing.router_logits(x, wg)
+    for t in range(T):
+        for e in range(E):
+            exact = sum(Fraction(float(x[t, h])) * Fraction(float(wg[e, h])) for h in range(H))
+            got = Fraction(float(logits[t, e]))
+            ulp = Fraction(float(np.spacing(np.float32(abs(float(exact))))))
+            assert abs(got - exact) <= ulp
+
+
+def test_router_rejects_mismatched_hidden_size():
+    with pytest.raises(ValueError):
+        routing.router_logits(np.zeros((2, 4)), np.zeros((3, 5), dtype=np.float32))

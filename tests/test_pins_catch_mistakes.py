@@ -35,6 +35,12 @@ MISTAKES = [
     ("routing.py", "ids = _rank_desc(masked)[:, :topk]", "ids = _rank_desc(xd)[:, :topk]", "group mask ignored"),
     ("routing.py", "sel_groups = _rank_desc(group_key)[:, :topk_group]",
      "sel_groups = _rank_desc(-group_key)[:, :topk_group]", "worst groups kept"),
+    ("routing.py", "    return (x @ w.T).astype(np.float32)", "    return (x @ w.T).astype(np.float16).astype(np.float32)",
+     "router logits rounded to half precision"),
+    ("routing.py", "    return (x @ w.T).astype(np.float32)",
+     "    return (x.astype(np.float32) @ w.T.astype(np.float32)).astype(np.float32)", "router summed in float32"),
+    ("routing.py", "    logits = router_logits(hidden_states, w_gate)\n",
+     "    logits = -router_logits(hidden_states, w_gate)\n", "router logits negated"),
     # align (mini-sglang moe_align_block_size)
     ("align.py", "sorted_ids = np.full(cap, num_pairs, dtype=np.int32)",
      "sorted_ids = np.full(cap, num_pairs - 1, dtype=np.int32)", "sentinel off by one"),
