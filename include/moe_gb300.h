@@ -325,6 +325,15 @@ MOE_API moe_status_t gmm_lowp(const void* input, const void* weights, const floa
  */
 MOE_API moe_status_t moe_check_device_error(void* ws, int* code, void* stream);
 
+/*
+ * moe_read_probe -- instrumentation, not in the pages: reads `bytes` bytes (a multiple
+ * of 16, 16-byte aligned) at `src` once with 16-byte loads over a grid of 8 CTAs per
+ * SM, and nothing else (*sink, one float, is written only for a sum no finite input
+ * of the benchmark produces). The benchmark times it beside the routing kernel on a
+ * buffer of the logits' size, as the device's streaming-read floor for those bytes.
+ */
+MOE_API moe_status_t moe_read_probe(const void* src, size_t bytes, float* sink, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 MOE_API const char* moe_status_string(int status);
 

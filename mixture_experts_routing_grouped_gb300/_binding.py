@@ -43,6 +43,7 @@ _SIGNATURES = {
     "gmm_lowp_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "gmm_lowp": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                           _c_size, _vp]),
+    "moe_read_probe": (_c_int, [_vp, _c_size, _vp, _vp]),
     "moe_check_device_error": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
     "moe_status_string": (ctypes.c_char_p, [_c_int]),
     "moe_set_stage_events": (None, [ctypes.POINTER(_vp), _c_int]),
@@ -368,3 +369,12 @@ def moe_check_device_error(ws: torch.Tensor) -> int:
     if st not in (MOE_OK, MOE_ERR_DEVICE_DATA):
         _check("moe_check_device_error", st)
     return int(code.value)
+
+
+def moe_read_probe(src: torch.Tensor, sink: torch.Tensor) -> None:
+    """Instrumentation: one streaming read of ``src``'s bytes on the current stream (the
+    benchmark's read floor)."""
+    _need(src, "src")
+    _need(sink, "sink", torch.float32)
+    st = lib().moe_read_probe(_ptr(src), src.numel() * src.element_size(), _ptr(sink), _stream(src))
+    _check("moe_read_probe", st)

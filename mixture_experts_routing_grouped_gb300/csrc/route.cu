@@ -26,7 +26,12 @@
 
 namespace moe {
 
+bool make_tmap_f32_32x32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
+
 namespace {
+
+// Below this many tokens the segmented kernels (a single wave, no pipeline to fill) are used.
+constexpr int kTptMinTokens = 2048;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t b = __float_as_uint(f);
@@ -568,6 +573,297 @@ __global__ void __launch_bounds__(kSegThreads, 6) grouped_topk_seg_kernel(const 
   }
 }
 
+// ----------------------------------------------------------------------------
+// Thread-per-token kernel for the common shapes (E = 128 or 256, whole 8-expert
+// units per group, topk = 8), fed by TMA.
+//
+// A persistent CTA per SM: one producer thread streams tiles of 32 tokens (their
+// [32, E] fp32 logits) into shared-memory stages with 2D tensor loads (boxes of 32
+// logits x 32 tokens, 128-byte swizzle, so that lane r reading its own row touches
+// eight distinct bank groups per quarter-warp), and six compute warps take the
+// tiles in turn, lane r of a warp selecting for token r of its tile; each warp owns
+// its own stages. The loads of the next tiles are in flight while the current ones
+// are selected.
+//
+// Per token (GroupedTopK blog 3.2-3.6, on the logits as in its section 七):
+//  1. maxima of every unit of 8 consecutive experts, and the group maxima from them;
+//  2. the group ranks (greater maximum first, equal maxima to the lower group), and
+//     the mask of the topk_group best groups;
+//  3. a lower bound tau of the topk-th largest candidate: the topk-th largest of the
+//     selected groups' unit maxima (distinct candidates, so at least topk are >= tau);
+//  4. the candidates >= tau (about topk + 2 on Gaussian logits) are marked in bit
+//     masks of the selected groups;
+//  5. the marked candidates, in increasing index, are inserted into a sorted register
+//     list of topk (value, index) pairs, strict comparisons keeping the lower index
+//     first among equal values (rows with many equal values near the top just mark
+//     more candidates).
+// The weights follow as in the other kernels.
+namespace tpt {
+
+constexpr int kTile = 32;
+constexpr int kComputeWarps = 6;
+constexpr int kThreads = (kComputeWarps + 1) * 32;
+constexpr int kK = 8;
+
+template <int E>
+struct Shape {
+  static constexpr int kBoxes = E / 32;                 // 128-byte column boxes per row
+  static constexpr int kUnits = E / 8;
+  static constexpr int kStageBytes = kTile * E * 4;     // 32 KB at E = 256
+  // each compute warp owns kDepth stages (one consumer per stage: its barriers are waited on in
+  // order by one warp, so no wait can match an older phase of the same parity)
+  static constexpr int kDepth = (192 * 1024) / kStageBytes / kComputeWarps > 0
+                                    ? (192 * 1024) / kStageBytes / kComputeWarps : 1;
+  static constexpr int kStages = kComputeWarps * kDepth;
+  static constexpr int kBarOff = kStages * kStageBytes;
+  static constexpr int kSmem = kBarOff + 2 * kStages * 8 + 16 + 1024;  // + alignment slack
+};
+
+// Shared address of logit e of lane-row r in a stage (see the swizzle above).
+template <int E>
+__device__ __forceinline__ uint32_t logit_addr(uint32_t stage, int r, int e) {
+  const int box = e >> 5, chunk = (e >> 2) & 7, word = e & 3;
+  return stage + box * 4096 + r * 128 + (((chunk ^ (r & 7)) << 4) | (word << 2));
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 lds_f32x4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+  return v;
+}
+
+// (x, ix) into the descending list (v, id) of kK entries; candidates arrive in
+// increasing index, so a strict comparison puts x after every equal value.
+__device__ __forceinline__ void insert_sorted(float (&v)[kK], int (&id)[kK], float x, int ix) {
+  bool c[kK];
+#pragma unroll
+  for (int i = 0; i < kK; ++i) c[i] = x > v[i];
+#pragma unroll
+  for (int i = kK - 1; i > 0; --i) {
+    const float vm = c[i - 1] ? v[i - 1] : x;
+    const int im = c[i - 1] ? id[i - 1] : ix;
+    v[i] = c[i] ? vm : v[i];
+    id[i] = c[i] ? im : id[i];
+  }
+  v[0] = c[0] ? x : v[0];
+  id[0] = c[0] ? ix : id[0];
+}
+
+template <int E, int G, int KG>
+__global__ void __launch_bounds__(kThreads, 1) grouped_topk_tpt_kernel(const __grid_constant__ CUtensorMap map,
+                                                                      int T, int ntiles, int scoring, int renorm,
+                                                                      float rsf, float* __restrict__ out_w,
+                                                                      int32_t* __restrict__ out_ids, int* err) {
+  using S = Shape<E>;
+  constexpr int P = E / G;              // experts per group
+  constexpr int UPG = P / 8;            // units per group
+  static_assert(P % 8 == 0, "groups of whole 8-expert units");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t bar_full = sbase + S::kBarOff;
+  const uint32_t bar_empty = bar_full + S::kStages * 8;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kBarOff + 2 * S::kStages * 8);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S::kStages; ++i) {
+      ptx::mbar_init(bar_full + 8 * i, 1);
+      ptx::mbar_init(bar_empty + 8 * i, 1);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kComputeWarps) {
+    // producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&map);
+      // CTA-local tile i goes to warp i % W, its l = i / W -th tile, stage (i % W) * D + l % D
+      auto stage_of = [](int i) { return (i % kComputeWarps) * S::kDepth + (i / kComputeWarps) % S::kDepth; };
+      auto use_of = [](int i) { return (i / kComputeWarps) / S::kDepth; };  // earlier uses of that stage
+      int issued = 0;
+      for (int i = 0;; ++i) {
+        const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+        if (tile >= ntiles) break;
+        const int s = stage_of(i);
+        if (use_of(i) > 0 && !ptx::mbar_wait(bar_empty + 8 * s, (use_of(i) - 1) & 1, abort_flag)) break;
+        ptx::mbar_arrive_expect_tx(bar_full + 8 * s, S::kStageBytes);
+        const uint32_t dst = sbase + s * S::kStageBytes;
+#pragma unroll
+        for (int b = 0; b < S::kBoxes; ++b) ptx::tma_load_2d(dst + b * 4096, &map, bar_full + 8 * s, b * 32, tile * kTile);
+        issued = i + 1;
+      }
+      // every issued copy has landed before the CTA may exit (a no-op unless a wait gave up);
+      // the last kStages tiles issued cover each stage once
+      for (int j = issued - S::kStages > 0 ? issued - S::kStages : 0; j < issued; ++j)
+        ptx::mbar_wait_drain(bar_full + 8 * stage_of(j), use_of(j) & 1);
+    }
+    return;
+  }
+
+  for (int l = 0;; ++l) {
+    const int i = l * kComputeWarps + warp;
+    const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+    if (tile >= ntiles) break;
+    const int s = warp * S::kDepth + l % S::kDepth;
+    if (!ptx::mbar_wait(bar_full + 8 * s, (l / S::kDepth) & 1, abort_flag)) {
+      if (lane == 0) report_error(err, MOE_DEVERR_TIMEOUT);
+      break;
+    }
+    const uint32_t stage = sbase + s * S::kStageBytes;
+    const int r = lane;
+
+    // 1. unit and group maxima
+    float um[S::kUnits];
+#pragma unroll
+    for (int b = 0; b < S::kBoxes; ++b) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 a = lds_f32x4(stage + b * 4096 + r * 128 + (((2 * u) ^ (r & 7)) << 4));
+        const float4 c = lds_f32x4(stage + b * 4096 + r * 128 + (((2 * u + 1) ^ (r & 7)) << 4));
+        um[b * 4 + u] = fmaxf(max3f(max3f(a.x, a.y, a.z), max3f(a.w, c.x, c.y), c.z), c.w);
+      }
+    }
+    float gm[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float m = um[g * UPG];
+#pragma unroll
+      for (int u = 1; u < UPG; ++u) m = fmaxf(m, um[g * UPG + u]);
+      gm[g] = m;
+    }
+    // 2. group ranks
+    uint32_t sel = (G == 32) ? 0xffffffffu : ((1u << G) - 1u);
+    if (KG < G) {
+      int rank[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) rank[g] = 0;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int h = g + 1; h < G; ++h) {
+          const bool h_first = gm[h] > gm[g];  // equal maxima: the lower group g goes first
+          rank[g] += h_first ? 1 : 0;
+          rank[h] += h_first ? 0 : 1;
+        }
+      sel = 0;
+#pragma unroll
+      for (int g = 0; g < G; ++g) sel |= (rank[g] < KG ? 1u : 0u) << g;
+    }
+    // 3. tau: the topk-th largest unit maximum among the selected groups' units (each unit
+    //    maximum is a distinct candidate, so at least topk candidates are >= tau)
+    float tau = -CUDART_INF_F;
+    if (KG * UPG >= kK) {
+      float t[kK];
+#pragma unroll
+      for (int q = 0; q < kK; ++q) t[q] = -CUDART_INF_F;
+#pragma unroll
+      for (int u = 0; u < S::kUnits; ++u) {
+        const float x = ((sel >> (u / UPG)) & 1u) ? um[u] : -CUDART_INF_F;
+#pragma unroll
+        for (int q = kK - 1; q > 0; --q) t[q] = fmaxf(t[q], fminf(t[q - 1], x));
+        t[0] = fmaxf(t[0], x);
+      }
+      tau = t[kK - 1];
+    }
+    // 4-5. per selected group (in increasing group order): a bit mask of its candidates >= tau,
+    //      then the marked candidates inserted in increasing index into the sorted top-k
+    float v[kK];
+    int id[kK];
+#pragma unroll
+    for (int q = 0; q < kK; ++q) { v[q] = -CUDART_INF_F; id[q] = 0x7fffffff; }
+    for (uint32_t rem = sel; rem; rem &= rem - 1) {
+      const int g = __ffs(rem) - 1;
+#pragma unroll 1
+      for (int w = 0; w < (P + 31) / 32; ++w) {
+        const int base = g * P + 32 * w;
+        uint32_t m = 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          if (32 * w + 4 * c >= P) break;
+          const int e0 = base + 4 * c;
+          const float4 f = lds_f32x4(stage + (e0 >> 5) * 4096 + r * 128 + ((((e0 >> 2) & 7) ^ (r & 7)) << 4));
+          m |= ((f.x >= tau ? 1u : 0u) | (f.y >= tau ? 2u : 0u) | (f.z >= tau ? 4u : 0u) | (f.w >= tau ? 8u : 0u))
+               << (4 * c);
+        }
+        while (m) {
+          const int e = base + __ffs(m) - 1;
+          m &= m - 1;
+          insert_sorted(v, id, lds_f32(logit_addr<E>(stage, r, e)), e);
+        }
+      }
+    }
+    // softmax without renormalisation needs the full denominator: read the row once more and
+    // add its E terms pairwise (depth log2(E): every term is positive, so the sum's relative
+    // error stays within that many roundings)
+    float den = 0.f, rmax = 0.f;
+    if (scoring == MOE_SCORE_SOFTMAX && !renorm) {
+      rmax = gm[0];
+#pragma unroll
+      for (int g = 1; g < G; ++g) rmax = fmaxf(rmax, gm[g]);
+      float bs[S::kBoxes];
+#pragma unroll
+      for (int b = 0; b < S::kBoxes; ++b) {
+        float cs[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 f = lds_f32x4(stage + b * 4096 + r * 128 + ((c ^ (r & 7)) << 4));
+          cs[c] = (expf(f.x - rmax) + expf(f.y - rmax)) + (expf(f.z - rmax) + expf(f.w - rmax));
+        }
+        bs[b] = ((cs[0] + cs[1]) + (cs[2] + cs[3])) + ((cs[4] + cs[5]) + (cs[6] + cs[7]));
+      }
+#pragma unroll
+      for (int h = S::kBoxes / 2; h >= 1; h /= 2)
+#pragma unroll
+        for (int b = 0; b < h; ++b) bs[b] += bs[b + h];
+      den = bs[0];
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
+
+    // 3.6: weights
+    float w[kK];
+    if (scoring == MOE_SCORE_SOFTMAX) {
+      if (renorm) {
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < kK; ++q) { w[q] = expf(v[q] - v[0]); sum += w[q]; }
+#pragma unroll
+        for (int q = 0; q < kK; ++q) w[q] = w[q] / sum;
+      } else {
+#pragma unroll
+        for (int q = 0; q < kK; ++q) w[q] = expf(v[q] - rmax) / den;
+      }
+    } else {
+      float sum = 0.f;
+#pragma unroll
+      for (int q = 0; q < kK; ++q) { w[q] = 1.0f / (1.0f + expf(-v[q])); sum += w[q]; }
+      if (renorm) {
+#pragma unroll
+        for (int q = 0; q < kK; ++q) w[q] = w[q] / sum;
+      }
+    }
+    const int token = tile * kTile + r;
+    if (token < T) {
+      float4* wp = reinterpret_cast<float4*>(out_w + static_cast<size_t>(token) * kK);
+      int4* ip = reinterpret_cast<int4*>(out_ids + static_cast<size_t>(token) * kK);
+      wp[0] = make_float4(w[0] * rsf, w[1] * rsf, w[2] * rsf, w[3] * rsf);
+      wp[1] = make_float4(w[4] * rsf, w[5] * rsf, w[6] * rsf, w[7] * rsf);
+      ip[0] = make_int4(id[0], id[1], id[2], id[3]);
+      ip[1] = make_int4(id[4], id[5], id[6], id[7]);
+    }
+  }
+}
+
+}  // namespace tpt
+
 // Lanes per token for the segmented kernel (8, 16 or 32), or 0 when it does not
 // apply: P = E / L must be 4, 8, 16 or 32, every group must span whole lanes
 // (G divides L) and the topk results must fit one per lane (topk <= L).
@@ -621,6 +917,22 @@ void launch_topk(const float* gating, int T, int E, int G, int kg, int k, int sc
   grouped_topk_kernel<VPL><<<blocks, threads, 0, s>>>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z);
 }
 
+// Thread-per-token kernel instances: (E, G, topk_group) with topk = 8.
+template <int E, int G, int KG>
+moe_status_t launch_tpt(const float* gating, int T, int scoring, int renorm, float rsf, float* w, int32_t* ids,
+                        cudaStream_t s) {
+  CUtensorMap map;
+  if (!make_tmap_f32_32x32(&map, gating, static_cast<uint64_t>(T), E)) return MOE_ERR_CUDA;
+  auto kernel = tpt::grouped_topk_tpt_kernel<E, G, KG>;
+  constexpr int smem = tpt::Shape<E>::kSmem;
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(kernel), smem)) return MOE_ERR_CUDA;
+  const int ntiles = cdiv(T, tpt::kTile);
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  const int grid = ntiles < sms ? ntiles : sms;
+  kernel<<<grid, tpt::kThreads, smem, s>>>(map, T, ntiles, scoring, renorm, rsf, w, ids, nullptr);
+  return launch_status();
+}
+
 }  // namespace
 
 moe_status_t validate_routing(int T, int E, int G, int kg, int k, int scoring) {
@@ -636,6 +948,12 @@ moe_status_t launch_grouped_topk(const float* gating, int T, int E, int G, int k
                                  int* zero_cnt, int cnt_per_row) {
   if (T == 0) return MOE_OK;
   const RouteZero z{reinterpret_cast<float4*>(zero_rows), zero_cols / 4, zero_cnt, cnt_per_row};
+  // the thread-per-token kernel: enough tokens to stream, no rows to clear, its shapes
+  if (!zero_rows && !zero_cnt && k == 8 && T >= kTptMinTokens && aligned16(w) && aligned16(ids)) {
+    if (E == 256 && G == 8 && kg == 4) return launch_tpt<256, 8, 4>(gating, T, scoring, renorm, rsf, w, ids, s);
+    if (E == 256 && G == 1) return launch_tpt<256, 1, 1>(gating, T, scoring, renorm, rsf, w, ids, s);
+    if (E == 128 && G == 1) return launch_tpt<128, 1, 1>(gating, T, scoring, renorm, rsf, w, ids, s);
+  }
   const int L = (G & (G - 1)) == 0 ? seg_lanes(E, G, k) : 0;
   if (L == 8) {
     switch (E / L) {

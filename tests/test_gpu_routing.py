@@ -71,3 +71,27 @@ def test_routing_T0_is_a_no_op():
     g = torch.empty((0, 256), dtype=torch.float32, device="cuda")
     w, ids = moe.moe_grouped_topk(g, 8, True, 8, 4, "softmax", 1.0)
     assert w.shape == (0, 8) and ids.shape == (0, 8)
+
+
+def _special_rows(E, rng):
+    rows = [np.zeros(E), np.full(E, 3.0), np.tile([5.0, 5.0, 1.0, 1.0], E // 4),
+            rng.integers(-3, 4, size=E).astype(float), rng.integers(-1, 2, size=E).astype(float),
+            np.where(np.arange(E) % 2 == 0, 30.0, -30.0), np.linspace(-20, 20, E), -np.linspace(-20, 20, E),
+            rng.normal(0, 1e-3, size=E), np.full(E, -0.0), np.repeat(rng.normal(0, 2, size=E // 8), 8),
+            np.where(np.arange(E) < 16, 7.0, rng.normal(0, 1, size=E))]
+    return np.array(rows, dtype=np.float32)
+
+
+@pytest.mark.parametrize("E,G,kg", [(256, 8, 4), (256, 1, 1), (128, 1, 1)])
+@pytest.mark.parametrize("T", [2048, 4095, 20000])
+@pytest.mark.parametrize("scoring", ["softmax", "sigmoid"])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_routing_streaming_shapes_with_special_rows(E, G, kg, T, scoring, renorm):
+    # T >= 2048 with topk = 8 selects the thread-per-token streaming kernel for these (E, G, topk_group);
+    # every 5th row is one of the tie-heavy special rows (the list of candidates overflows on several)
+    rng = np.random.default_rng(E + T + G)
+    x = rng.normal(0, 2, size=(T, E)).astype(np.float32)
+    sp = _special_rows(E, rng)
+    idx = np.arange(0, T, 5)
+    x[idx] = sp[np.arange(idx.size) % len(sp)]
+    _run(x, 8, renorm, G, kg, scoring, 2.5)
