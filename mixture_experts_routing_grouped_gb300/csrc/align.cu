@@ -236,11 +236,14 @@ __global__ void __launch_bounds__(kAlignThreads)
   for (int e = tid; e < E; e += kAlignThreads) hists[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
 }
 
+// The histogram rows may be finer than the chunks (rows_per_chunk rows of chunk /
+// rows_per_chunk pairs each, e.g. the per-tile counts written by the routing kernel).
 __global__ void __launch_bounds__(kAlignThreads)
     align_scan_scatter_kernel(const int32_t* __restrict__ ids, int num_pairs, int E, int block_m, int cap, int chunk,
-                              int nchunks, const int32_t* __restrict__ hists, int32_t* __restrict__ sorted_ids,
-                              int32_t* __restrict__ sorted_tok, int topk, int32_t* __restrict__ expert_ids,
-                              int32_t* __restrict__ expert_offsets, int32_t* __restrict__ ntpp) {
+                              int nchunks, const int32_t* __restrict__ hists, int nrows, int rows_per_chunk,
+                              int32_t* __restrict__ sorted_ids, int32_t* __restrict__ sorted_tok, int topk,
+                              int32_t* __restrict__ expert_ids, int32_t* __restrict__ expert_offsets,
+                              int32_t* __restrict__ ntpp, int* __restrict__ zero_word) {
   extern __shared__ int sm[];
   int* cur = sm;                              // [kAlignWarps][E] write cursors
   int* tot = cur + kAlignWarps * E;           // [E] pairs per expert
@@ -249,15 +252,25 @@ __global__ void __launch_bounds__(kAlignThreads)
   __shared__ int warp_tot[kAlignWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
+  if (zero_word && blockIdx.x == 0 && tid == 0) *zero_word = 0;
   for (int i = tid; i < (kAlignWarps + 2) * E; i += kAlignThreads) sm[i] = 0;
   __syncthreads();
-  const int n_h = nchunks * E;
-  for (int idx = tid; idx < n_h; idx += kAlignThreads) {
-    const int v = __ldcg(hists + idx);
-    if (v) {
-      const int c = idx / E, e = idx - c * E;
-      atomicAdd(&tot[e], v);
-      if (c < static_cast<int>(blockIdx.x)) atomicAdd(&bef[e], v);
+  // per-expert totals and counts in earlier chunks: thread (part, e) sums rows part, part + parts, ...
+  // in registers, then the parts meet in shared memory (parts atomics per expert)
+  {
+    const int parts = kAlignThreads / E > 0 ? kAlignThreads / E : 1;
+    const int part = tid / E, e = tid - part * E;
+    if (part < parts) {
+      const int split = static_cast<int>(blockIdx.x) * rows_per_chunk;  // rows before this chunk
+      int t_sum = 0, b_sum = 0;
+#pragma unroll 4
+      for (int row = part; row < nrows; row += parts) {
+        const int v = __ldcg(hists + static_cast<size_t>(row) * E + e);
+        t_sum += v;
+        b_sum += row < split ? v : 0;
+      }
+      if (t_sum) atomicAdd(&tot[e], t_sum);
+      if (b_sum) atomicAdd(&bef[e], b_sum);
     }
   }
   __syncthreads();
@@ -379,8 +392,8 @@ moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m,
                           static_cast<int>(static_cast<size_t>(kAlignWarps + 3) * MOE_MAX_EXPERTS * sizeof(int))))
       return MOE_ERR_CUDA;
     align_scan_scatter_kernel<<<p.nchunks, kAlignThreads, smem, s>>>(
-        ids, num_pairs, E, block_m, cap, p.chunk, p.nchunks, chunk_base, sorted_ids, sorted_tok,
-        topk > 0 ? topk : 1, expert_ids, expert_offsets, ntpp);
+        ids, num_pairs, E, block_m, cap, p.chunk, p.nchunks, chunk_base, p.nchunks, 1, sorted_ids, sorted_tok,
+        topk > 0 ? topk : 1, expert_ids, expert_offsets, ntpp, nullptr);
     return launch_status();
   }
   align_count_scan_kernel<<<p.nchunks, kAlignThreads, 0, s>>>(ids, num_pairs, E, block_m, cap, p.chunk, p.nchunks,
@@ -394,6 +407,42 @@ moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m,
     return MOE_ERR_CUDA;
   align_scatter_kernel<<<p.nchunks, kAlignThreads, smem, s>>>(ids, num_pairs, E, p.chunk, chunk_base, done,
                                                               sorted_ids, sorted_tok, topk > 0 ? topk : 1);
+  return launch_status();
+}
+
+// Scratch for align run on the routing kernel's counts of T tokens: 256 bytes, then at most
+// kSmallScan counts (rows of at least 4 tokens; align takes no more).
+size_t align_tile_hist_bytes(int T, int E) {
+  const long long n = std::min(static_cast<long long>((T + 3) / 4) * E, static_cast<long long>(kSmallScan));
+  return 256 + align_up(static_cast<size_t>(n) * 4, 256);
+}
+
+// Whether the single-pass align can take tile_rows rows of pair_per_tile pairs instead of
+// counting the pairs itself: every chunk is a whole number of rows, and the rows fit the
+// single-pass scan.
+bool align_takes_tile_hists(int num_pairs, int E, int tile_rows, int pairs_per_tile) {
+  const AlignPlan p = align_plan(num_pairs);
+  return pairs_per_tile > 0 && p.chunk % pairs_per_tile == 0 &&
+         static_cast<long long>(tile_rows) * E <= kSmallScan && p.nchunks * E <= kSmallScan;
+}
+
+// Align with the first pass already done: tile_hist (in scratch, after its 256-byte
+// header) holds tile_rows rows of per-expert counts of consecutive runs of
+// pairs_per_tile pairs (the routing kernel's tiles). Also zeroes *zero_word.
+moe_status_t launch_align_from_tile_hists(const int32_t* ids, int num_pairs, int E, int block_m,
+                                          int32_t* sorted_ids, int32_t* expert_ids, int32_t* expert_offsets,
+                                          int32_t* ntpp, const int32_t* tile_hist, int tile_rows,
+                                          int pairs_per_tile, cudaStream_t s, int32_t* sorted_tok, int topk,
+                                          int* zero_word) {
+  const int cap = static_cast<int>(align_max_padded(num_pairs, E, block_m));
+  const AlignPlan p = align_plan(num_pairs);
+  const size_t smem = static_cast<size_t>(kAlignWarps + 3) * E * sizeof(int);
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(align_scan_scatter_kernel),
+                        static_cast<int>(static_cast<size_t>(kAlignWarps + 3) * MOE_MAX_EXPERTS * sizeof(int))))
+    return MOE_ERR_CUDA;
+  align_scan_scatter_kernel<<<p.nchunks, kAlignThreads, smem, s>>>(
+      ids, num_pairs, E, block_m, cap, p.chunk, p.nchunks, tile_hist, tile_rows, p.chunk / pairs_per_tile,
+      sorted_ids, sorted_tok, topk > 0 ? topk : 1, expert_ids, expert_offsets, ntpp, zero_word);
   return launch_status();
 }
 

@@ -17,6 +17,19 @@ moe_status_t validate_routing(int T, int E, int G, int kg, int k, int scoring);
 moe_status_t launch_grouped_topk(const float* gating, int T, int E, int G, int kg, int k, int scoring, int renorm,
                                  float rsf, float* w, int32_t* ids, cudaStream_t s, float* zero_rows, int zero_cols,
                                  int* zero_cnt, int cnt_per_row);
+moe_status_t launch_grouped_topk_tile_hist(const float* gating, int T, int E, int G, int kg, int k, int scoring,
+                                           int renorm, float rsf, float* w, int32_t* ids, int32_t* tile_hist,
+                                           int* err, float* zero_rows, int zero_cols, int* rows_out,
+                                           int* tokens_per_row, cudaStream_t s);
+int route_hist_rows(int T, int E, int G, int kg, int k, const void* w, const void* ids, bool zero_rows,
+                    int* tokens_per_row);
+size_t align_tile_hist_bytes(int T, int E);
+bool align_takes_tile_hists(int num_pairs, int E, int tile_rows, int pairs_per_tile);
+moe_status_t launch_align_from_tile_hists(const int32_t* ids, int num_pairs, int E, int block_m,
+                                          int32_t* sorted_ids, int32_t* expert_ids, int32_t* expert_offsets,
+                                          int32_t* ntpp, const int32_t* tile_hist, int tile_rows,
+                                          int pairs_per_tile, cudaStream_t s, int32_t* sorted_tok, int topk,
+                                          int* zero_word);
 size_t align_max_padded(int num_pairs, int E, int block_m);
 size_t align_scratch_bytes(int num_pairs, int E);
 moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m, int32_t* sorted_ids,
@@ -101,7 +114,8 @@ FusedLayout fused_layout(int T, int H, int I, int E, int topk, int block_m) {
   const int num_pairs = T * topk;
   L.cap = static_cast<int>(align_max_padded(num_pairs, E, block_m));
   size_t off = kWsHeader;
-  L.align_scratch = off; off = align_up(off + align_scratch_bytes(num_pairs, E), 256);
+  const size_t own = align_scratch_bytes(num_pairs, E), tiles = align_tile_hist_bytes(T, E);
+  L.align_scratch = off; off = align_up(off + (own > tiles ? own : tiles), 256);
   L.sorted_ids = off; off = align_up(off + static_cast<size_t>(L.cap) * 4, 256);
   L.sorted_tok = off; off = align_up(off + static_cast<size_t>(L.cap) * 4, 256);
   L.expert_ids = off; off = align_up(off + static_cast<size_t>(L.cap / block_m + 1) * 4, 256);
@@ -176,6 +190,40 @@ int grid_for(size_t n4) {
   return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
+// Routing, then align, on stream s. Where the routing kernel for this shape can count the
+// experts of its rows of tokens (the segmented and streaming kernels) and align can start
+// from those counts, routing writes them into the align scratch and align skips its own
+// counting pass (one launch fewer).
+moe_status_t route_and_align(const float* gating, int T, int E, int G, int kg, int topk, int scoring, int renorm,
+                             float rsf, float* topk_weights, int32_t* topk_ids, float* zero_rows, int zero_cols,
+                             int block_m, int32_t* sorted_ids, int32_t* expert_ids, int32_t* offsets, int32_t* ntpp,
+                             uint8_t* align_scratch, int* err, int32_t* sorted_tok, int* tile_counter,
+                             cudaStream_t s) {
+  const int num_pairs = T * topk;
+  int32_t* tile_hist = reinterpret_cast<int32_t*>(align_scratch + 256);
+  int tpr = 0;
+  int rows = route_hist_rows(T, E, G, kg, topk, topk_weights, topk_ids, zero_rows != nullptr, &tpr);
+  if (rows > 0 && !align_takes_tile_hists(num_pairs, E, rows, tpr * topk)) rows = 0;
+  moe_status_t st;
+  if (rows > 0) {
+    int launched = 0;
+    st = launch_grouped_topk_tile_hist(gating, T, E, G, kg, topk, scoring, renorm, rsf, topk_weights, topk_ids,
+                                       tile_hist, err, zero_rows, zero_cols, &launched, &tpr, s);
+    if (st != MOE_OK) return st;
+    if (launched != rows) return MOE_ERR_CUDA;  // the two choices of kernel disagree (cannot happen)
+  } else {
+    st = launch_grouped_topk(gating, T, E, G, kg, topk, scoring, renorm, rsf, topk_weights, topk_ids, s, zero_rows,
+                             zero_cols, nullptr, 0);
+    if (st != MOE_OK) return st;
+  }
+  stage_mark(1, s);
+  if (rows > 0)
+    return launch_align_from_tile_hists(topk_ids, num_pairs, E, block_m, sorted_ids, expert_ids, offsets, ntpp,
+                                        tile_hist, rows, tpr * topk, s, sorted_tok, topk, tile_counter);
+  return launch_align(topk_ids, num_pairs, E, block_m, sorted_ids, expert_ids, offsets, ntpp, align_scratch, err, s,
+                      sorted_tok, topk, tile_counter);
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -229,13 +277,9 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
   // kernel (each token's row).
   const bool gate_up_clears = !plan.swap;
   stage_mark(0, s);
-  st = launch_grouped_topk(gating, T, E, num_expert_group, topk_group, topk, scoring, renormalize,
-                           routed_scaling_factor, topk_weights, topk_ids, s, gate_up_clears ? nullptr : y_acc, H,
-                           nullptr, 0);
-  if (st != MOE_OK) return st;
-  stage_mark(1, s);
-  st = launch_align(topk_ids, num_pairs, E, plan.block_m, sorted_ids, expert_ids, offsets, ntpp, w + L.align_scratch,
-                    err, s, sorted_tok, topk, tile_counter);
+  st = route_and_align(gating, T, E, num_expert_group, topk_group, topk, scoring, renormalize, routed_scaling_factor,
+                       topk_weights, topk_ids, gate_up_clears ? nullptr : y_acc, H, plan.block_m, sorted_ids,
+                       expert_ids, offsets, ntpp, w + L.align_scratch, err, sorted_tok, tile_counter, s);
   if (st != MOE_OK) return st;
   stage_mark(2, s);
   const size_t n4 = static_cast<size_t>(T) * H / 4;
@@ -320,12 +364,9 @@ extern "C" moe_status_t moe_fused_forward_fp8(const void* x, const float* gating
     if (st != MOE_OK) return st;
     if (cudaEventRecord(side->join, side->st) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  st = launch_grouped_topk(gating, T, E, num_expert_group, topk_group, topk, scoring, renormalize,
-                           routed_scaling_factor, topk_weights, topk_ids, s, nullptr, H, nullptr, 0);
-  if (st != MOE_OK) return st;
-  stage_mark(1, s);
-  st = launch_align(topk_ids, num_pairs, E, 128, sorted_ids, expert_ids, offsets, ntpp, w + L.base.align_scratch,
-                    err, s, sorted_tok, topk, tile_counter);
+  st = route_and_align(gating, T, E, num_expert_group, topk_group, topk, scoring, renormalize, routed_scaling_factor,
+                       topk_weights, topk_ids, nullptr, H, 128, sorted_ids, expert_ids, offsets, ntpp,
+                       w + L.base.align_scratch, err, sorted_tok, tile_counter, s);
   if (st != MOE_OK) return st;
   stage_mark(2, s);
   if (side) {

@@ -30,8 +30,8 @@ bool make_tmap_f32_32x32(CUtensorMap* map, const void* base, uint64_t rows, uint
 
 namespace {
 
-// Below this many tokens the segmented kernels (a single wave, no pipeline to fill) are used.
-constexpr int kTptMinTokens = 2048;
+// Below this many tokens the segmented kernels (a single wave, no pipeline to fill) are faster.
+constexpr int kTptMinTokens = 8192;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t b = __float_as_uint(f);
@@ -57,6 +57,8 @@ struct RouteZero {
   int row_f4;      // float4s per token row
   int* cnt;
   int cnt_per_row;
+  int32_t* hist;   // segmented kernel: one row of E expert counts per CTA (null: none)
+  int* err;        // device error word for ids the counts cannot take (null: none)
 };
 
 __device__ __forceinline__ void zero_token_rows(const RouteZero& z, int token, int lane) {
@@ -388,6 +390,7 @@ __global__ void __launch_bounds__(kSegThreads, 6) grouped_topk_seg_kernel(const 
   constexpr uint32_t kSwzMask = kRowBytes >= 32 ? kRowBytes / 16 - 1 : 0;
   if (K > 0) topk = K;
   __shared__ __align__(1024) uint8_t rows[kSegThreads * kRowBytes];
+  __shared__ int hist_s[P * L];
   const int tid = threadIdx.x;
   const uint32_t base = ptx::smem_u32(rows);
   auto chunk_addr = [&](int row, int j) {  // shared address of 16-byte chunk j of lane-row `row`
@@ -571,6 +574,19 @@ __global__ void __launch_bounds__(kSegThreads, 6) grouped_topk_seg_kernel(const 
       for (int i = s; i < zero.cnt_per_row; i += L) c[i] = 0;
     }
   }
+  // the CTA's expert counts (align's first pass over its tokens' pairs), when asked for
+  if (zero.hist) {
+    constexpr int E = P * L;
+    for (int e = tid; e < E; e += kSegThreads) hist_s[e] = 0;
+    __syncthreads();
+    if (token < T && active) {
+      if (static_cast<unsigned>(my_id) < static_cast<unsigned>(E)) atomicAdd(&hist_s[my_id], 1);
+      else report_error(zero.err, MOE_DEVERR_EXPERT_ID);
+    }
+    __syncthreads();
+    int32_t* row_out = zero.hist + static_cast<size_t>(blockIdx.x) * E;
+    for (int e = tid; e < E; e += kSegThreads) row_out[e] = hist_s[e];
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -616,7 +632,8 @@ struct Shape {
                                     ? (192 * 1024) / kStageBytes / kComputeWarps : 1;
   static constexpr int kStages = kComputeWarps * kDepth;
   static constexpr int kBarOff = kStages * kStageBytes;
-  static constexpr int kSmem = kBarOff + 2 * kStages * 8 + 16 + 1024;  // + alignment slack
+  static constexpr int kHistOff = kBarOff + 2 * kStages * 8 + 16;      // per-warp expert counts
+  static constexpr int kSmem = kHistOff + kComputeWarps * E * 4 + 1024;  // + alignment slack
 };
 
 // Shared address of logit e of lane-row r in a stage (see the swizzle above).
@@ -658,7 +675,8 @@ template <int E, int G, int KG>
 __global__ void __launch_bounds__(kThreads, 1) grouped_topk_tpt_kernel(const __grid_constant__ CUtensorMap map,
                                                                       int T, int ntiles, int scoring, int renorm,
                                                                       float rsf, float* __restrict__ out_w,
-                                                                      int32_t* __restrict__ out_ids, int* err) {
+                                                                      int32_t* __restrict__ out_ids, int* err,
+                                                                      int32_t* __restrict__ tile_hist) {
   using S = Shape<E>;
   constexpr int P = E / G;              // experts per group
   constexpr int UPG = P / 8;            // units per group
@@ -828,26 +846,29 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_topk_tpt_kernel(const __g
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
 
-    // 3.6: weights
+    // 3.6: weights (one reciprocal of the sum; each sigmoid as the correctly rounded 1 / (1 + e^-x))
     float w[kK];
     if (scoring == MOE_SCORE_SOFTMAX) {
       if (renorm) {
         float sum = 0.f;
 #pragma unroll
         for (int q = 0; q < kK; ++q) { w[q] = expf(v[q] - v[0]); sum += w[q]; }
+        const float inv = 1.0f / sum;
 #pragma unroll
-        for (int q = 0; q < kK; ++q) w[q] = w[q] / sum;
+        for (int q = 0; q < kK; ++q) w[q] *= inv;
       } else {
+        const float inv = 1.0f / den;
 #pragma unroll
-        for (int q = 0; q < kK; ++q) w[q] = expf(v[q] - rmax) / den;
+        for (int q = 0; q < kK; ++q) w[q] = expf(v[q] - rmax) * inv;
       }
     } else {
       float sum = 0.f;
 #pragma unroll
-      for (int q = 0; q < kK; ++q) { w[q] = 1.0f / (1.0f + expf(-v[q])); sum += w[q]; }
+      for (int q = 0; q < kK; ++q) { w[q] = __frcp_rn(1.0f + expf(-v[q])); sum += w[q]; }
       if (renorm) {
+        const float inv = 1.0f / sum;
 #pragma unroll
-        for (int q = 0; q < kK; ++q) w[q] = w[q] / sum;
+        for (int q = 0; q < kK; ++q) w[q] *= inv;
       }
     }
     const int token = tile * kTile + r;
@@ -858,6 +879,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_topk_tpt_kernel(const __g
       wp[1] = make_float4(w[4] * rsf, w[5] * rsf, w[6] * rsf, w[7] * rsf);
       ip[0] = make_int4(id[0], id[1], id[2], id[3]);
       ip[1] = make_int4(id[4], id[5], id[6], id[7]);
+    }
+    // the tile's expert counts (align's first pass over these pairs), when asked for
+    if (tile_hist) {
+      int* wh = reinterpret_cast<int*>(smem + S::kHistOff) + warp * E;
+      for (int e = lane; e < E; e += 32) wh[e] = 0;
+      __syncwarp();
+      if (token < T) {
+#pragma unroll
+        for (int q = 0; q < kK; ++q) {
+          if (static_cast<unsigned>(id[q]) < static_cast<unsigned>(E)) atomicAdd(&wh[id[q]], 1);
+          else report_error(err, MOE_DEVERR_EXPERT_ID);
+        }
+      }
+      __syncwarp();
+      int32_t* row_out = tile_hist + static_cast<size_t>(tile) * E;
+      for (int e = lane; e < E; e += 32) row_out[e] = wh[e];
+      __syncwarp();
     }
   }
 }
@@ -920,7 +958,7 @@ void launch_topk(const float* gating, int T, int E, int G, int kg, int k, int sc
 // Thread-per-token kernel instances: (E, G, topk_group) with topk = 8.
 template <int E, int G, int KG>
 moe_status_t launch_tpt(const float* gating, int T, int scoring, int renorm, float rsf, float* w, int32_t* ids,
-                        cudaStream_t s) {
+                        cudaStream_t s, int* err = nullptr, int32_t* tile_hist = nullptr) {
   CUtensorMap map;
   if (!make_tmap_f32_32x32(&map, gating, static_cast<uint64_t>(T), E)) return MOE_ERR_CUDA;
   auto kernel = tpt::grouped_topk_tpt_kernel<E, G, KG>;
@@ -929,11 +967,76 @@ moe_status_t launch_tpt(const float* gating, int T, int scoring, int renorm, flo
   const int ntiles = cdiv(T, tpt::kTile);
   const int sms = num_sms() > 0 ? num_sms() : 148;
   const int grid = ntiles < sms ? ntiles : sms;
-  kernel<<<grid, tpt::kThreads, smem, s>>>(map, T, ntiles, scoring, renorm, rsf, w, ids, nullptr);
+  kernel<<<grid, tpt::kThreads, smem, s>>>(map, T, ntiles, scoring, renorm, rsf, w, ids, err, tile_hist);
   return launch_status();
 }
 
+bool tpt_applies(int T, int E, int G, int kg, int k, const void* w, const void* ids) {
+  if (k != 8 || T < kTptMinTokens || !aligned16(w) || !aligned16(ids)) return false;
+  return (E == 256 && G == 8 && kg == 4) || (E == 256 && G == 1) || (E == 128 && G == 1);
+}
+
 }  // namespace
+
+// Routing that also writes the expert counts of every run of *tokens_per_row consecutive
+// tokens (rows of E int32 at tile_hist: align's first pass over those pairs): the
+// streaming kernel's 32-token tiles, or the segmented kernel's CTAs (rows_out rows).
+// *rows_out = 0 (nothing launched) for the shapes of the other kernels, and the caller
+// routes and counts the usual way. zero_rows / zero_cols: as for launch_grouped_topk
+// (segmented kernel only).
+moe_status_t launch_grouped_topk_tile_hist(const float* gating, int T, int E, int G, int kg, int k, int scoring,
+                                           int renorm, float rsf, float* w, int32_t* ids, int32_t* tile_hist,
+                                           int* err, float* zero_rows, int zero_cols, int* rows_out,
+                                           int* tokens_per_row, cudaStream_t s) {
+  *rows_out = 0;
+  if (T == 0) return MOE_OK;
+  if (!zero_rows && tpt_applies(T, E, G, kg, k, w, ids)) {
+    *rows_out = cdiv(T, tpt::kTile);
+    *tokens_per_row = tpt::kTile;
+    if (E == 256 && G == 8) return launch_tpt<256, 8, 4>(gating, T, scoring, renorm, rsf, w, ids, s, err, tile_hist);
+    if (E == 256) return launch_tpt<256, 1, 1>(gating, T, scoring, renorm, rsf, w, ids, s, err, tile_hist);
+    return launch_tpt<128, 1, 1>(gating, T, scoring, renorm, rsf, w, ids, s, err, tile_hist);
+  }
+  const int L = (G & (G - 1)) == 0 ? seg_lanes(E, G, k) : 0;
+  if (L == 0) return MOE_OK;
+  const RouteZero z{reinterpret_cast<float4*>(zero_rows), zero_cols / 4, nullptr, 0, tile_hist, err};
+  *tokens_per_row = kSegThreads / L;
+  *rows_out = cdiv(T, kSegThreads / L);
+  const int P = E / L;
+  if (L == 8) {
+    if (P == 4) return launch_seg<4, 8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+    if (P == 8) return launch_seg<8, 8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+    if (P == 16) return launch_seg<16, 8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+    if (P == 32) return launch_seg<32, 8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  } else if (L == 16) {
+    if (P == 16) return launch_seg<16, 16>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+    if (P == 32) return launch_seg<32, 16>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  } else if (L == 32) {
+    if (P == 16) return launch_seg<16, 32>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+    if (P == 32) return launch_seg<32, 32>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  }
+  *rows_out = 0;
+  return MOE_OK;
+}
+
+// The rows of counts launch_grouped_topk_tile_hist writes for this problem (0: none), and
+// the tokens of each row.
+int route_hist_rows(int T, int E, int G, int kg, int k, const void* w, const void* ids, bool zero_rows,
+                    int* tokens_per_row) {
+  if (T == 0) return 0;
+  if (!zero_rows && tpt_applies(T, E, G, kg, k, w, ids)) {
+    *tokens_per_row = tpt::kTile;
+    return cdiv(T, tpt::kTile);
+  }
+  const int L = (G & (G - 1)) == 0 ? seg_lanes(E, G, k) : 0;
+  if (L == 0) return 0;
+  const int P = E / L;
+  const bool inst = (L == 8 && (P == 4 || P == 8 || P == 16 || P == 32)) || (L == 16 && (P == 16 || P == 32)) ||
+                    (L == 32 && (P == 16 || P == 32));
+  if (!inst) return 0;
+  *tokens_per_row = kSegThreads / L;
+  return cdiv(T, kSegThreads / L);
+}
 
 moe_status_t validate_routing(int T, int E, int G, int kg, int k, int scoring) {
   if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || G < 1 || G > 32 || E % G != 0) return MOE_ERR_INVALID_ARG;
@@ -947,12 +1050,12 @@ moe_status_t launch_grouped_topk(const float* gating, int T, int E, int G, int k
                                  float rsf, float* w, int32_t* ids, cudaStream_t s, float* zero_rows, int zero_cols,
                                  int* zero_cnt, int cnt_per_row) {
   if (T == 0) return MOE_OK;
-  const RouteZero z{reinterpret_cast<float4*>(zero_rows), zero_cols / 4, zero_cnt, cnt_per_row};
+  const RouteZero z{reinterpret_cast<float4*>(zero_rows), zero_cols / 4, zero_cnt, cnt_per_row, nullptr, nullptr};
   // the thread-per-token kernel: enough tokens to stream, no rows to clear, its shapes
-  if (!zero_rows && !zero_cnt && k == 8 && T >= kTptMinTokens && aligned16(w) && aligned16(ids)) {
-    if (E == 256 && G == 8 && kg == 4) return launch_tpt<256, 8, 4>(gating, T, scoring, renorm, rsf, w, ids, s);
-    if (E == 256 && G == 1) return launch_tpt<256, 1, 1>(gating, T, scoring, renorm, rsf, w, ids, s);
-    if (E == 128 && G == 1) return launch_tpt<128, 1, 1>(gating, T, scoring, renorm, rsf, w, ids, s);
+  if (!zero_rows && !zero_cnt && tpt_applies(T, E, G, kg, k, w, ids)) {
+    if (E == 256 && G == 8) return launch_tpt<256, 8, 4>(gating, T, scoring, renorm, rsf, w, ids, s);
+    if (E == 256) return launch_tpt<256, 1, 1>(gating, T, scoring, renorm, rsf, w, ids, s);
+    return launch_tpt<128, 1, 1>(gating, T, scoring, renorm, rsf, w, ids, s);
   }
   const int L = (G & (G - 1)) == 0 ? seg_lanes(E, G, k) : 0;
   if (L == 8) {
