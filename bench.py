@@ -334,7 +334,8 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "e2e": {"value": round(job_tokens_per_s(cfg.T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": 6 * K,  # per step: routing, align histogram, align scan + scatter, gate_up, down, cast
+        # per step: routing (which also counts each row block's experts), align scan + scatter, gate_up, down, cast
+        "gpu_launches": 5 * K,
         "clocks": clk,
     }
     if not args.skip_extra and world == 1:
@@ -558,7 +559,7 @@ def bench_fp8_layer(moe, torch, dev, flush, peaks, args, cfg, acts, W):
             "peak_source": "2 x bf16_tflops (burst) of measured: the nominal fp8 / bf16 dense ratio",
             "traffic_bytes_per_launch": {"gemm_gate_up": kernel_traffic("pair::moe_gate_up_kernel<1>"),
                                          "gemm_down": kernel_traffic("moe_down_kernel<1>")},
-            "gpu_launches_per_step": 8}
+            "gpu_launches_per_step": 7}  # routing, align, quant x (side stream), gate_up, quant h, down, cast
 
 
 def bench_cublas_context(torch, dev, flush, cfg, ids, args):

@@ -334,6 +334,17 @@ MOE_API moe_status_t moe_check_device_error(void* ws, int* code, void* stream);
  */
 MOE_API moe_status_t moe_read_probe(const void* src, size_t bytes, float* sink, void* stream);
 
+/*
+ * moe_wait_timeout_probe -- test of the device-side failure detection, not in the pages:
+ * launches one CTA whose first warp waits on an on-chip barrier that nothing completes,
+ * with the same bounded wait every GEMM kernel uses but a limit of limit_ns (1 ..
+ * 2e9 ns), so that it runs out; the warp then raises the CTA's abort flag, a second
+ * warp waiting with the full limit leaves through that flag, and MOE_DEVERR_TIMEOUT is
+ * ORed into the error word at ws[0..4) (read it with moe_check_device_error). Nothing is
+ * in flight when the kernel returns; the context stays usable.
+ */
+MOE_API moe_status_t moe_wait_timeout_probe(void* ws, unsigned long long limit_ns, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 MOE_API const char* moe_status_string(int status);
 

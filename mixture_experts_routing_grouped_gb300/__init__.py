@@ -12,6 +12,6 @@ from ._binding import (  # noqa: F401
     moe_align_block_size, moe_align_max_padded, moe_check_device_error, moe_fused_forward,
     moe_fused_forward_fp8, moe_fused_forward_fp8_workspace_size,
     moe_fused_forward_noalloc, moe_fused_forward_noalloc_check_error, moe_fused_forward_workspace_size, moe_grouped_topk, moe_quant_per_token, moe_read_probe, moe_router_topk,
-    moe_router_topk_workspace_size, moe_set_stage_events,
+    moe_router_topk_workspace_size, moe_set_stage_events, moe_wait_timeout_probe,
     status_string,
 )

@@ -44,6 +44,7 @@ _SIGNATURES = {
     "gmm_lowp": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                           _c_size, _vp]),
     "moe_read_probe": (_c_int, [_vp, _c_size, _vp, _vp]),
+    "moe_wait_timeout_probe": (_c_int, [_vp, ctypes.c_ulonglong, _vp]),
     "moe_check_device_error": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
     "moe_status_string": (ctypes.c_char_p, [_c_int]),
     "moe_set_stage_events": (None, [ctypes.POINTER(_vp), _c_int]),
@@ -378,3 +379,10 @@ def moe_read_probe(src: torch.Tensor, sink: torch.Tensor) -> None:
     _need(sink, "sink", torch.float32)
     st = lib().moe_read_probe(_ptr(src), src.numel() * src.element_size(), _ptr(sink), _stream(src))
     _check("moe_read_probe", st)
+
+
+def moe_wait_timeout_probe(ws: torch.Tensor, limit_ns: int) -> None:
+    """Test of failure detection: one kernel whose bounded wait runs out after limit_ns and
+    reports MOE_DEVERR_TIMEOUT into ws's error word (read it with moe_check_device_error)."""
+    _need(ws, "ws")
+    _check("moe_wait_timeout_probe", lib().moe_wait_timeout_probe(_ptr(ws), int(limit_ns), _stream(ws)))

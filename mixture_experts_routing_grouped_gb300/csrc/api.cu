@@ -1,6 +1,7 @@
 // Host-side services shared by every entry point: device attributes, launch
 // status, kernel attributes, the device error word and status names.
 #include "common.cuh"
+#include "ptx.cuh"
 
 #include <mutex>
 #include <map>
@@ -59,8 +60,39 @@ __global__ void __launch_bounds__(256) read_probe_kernel(const float4* __restric
   if (acc == -1234567.0f) *sink = acc;
 }
 
+// The kernels' bounded wait, run out on purpose: warp 0 waits on an mbarrier that
+// nothing arrives on for limit_ns, then raises the CTA's abort flag and reports
+// MOE_DEVERR_TIMEOUT; warp 1 waits on a second such barrier with the kernels' full
+// limit and must leave early through the abort flag (as the other roles of a GEMM
+// CTA do). No copy, MMA or tensor memory is in flight; the kernel returns.
+__global__ void __launch_bounds__(64) wait_probe_kernel(int* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bars[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars[1]), 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  volatile int* ab = &abort_flag;
+  if (lane == 0) {
+    const bool ok = warp == 0 ? ptx::mbar_wait_for(ptx::smem_u32(&bars[0]), 0, ab, limit_ns)
+                              : ptx::mbar_wait(ptx::smem_u32(&bars[1]), 0, ab);
+    if (!ok && warp == 0) report_error(err, MOE_DEVERR_TIMEOUT);
+  }
+  __syncthreads();
+}
+
 }  // namespace
 }  // namespace moe
+
+extern "C" moe_status_t moe_wait_timeout_probe(void* ws, unsigned long long limit_ns, void* stream) {
+  if (!ws || limit_ns == 0 || limit_ns > moe::ptx::kWaitLimitNs) return MOE_ERR_INVALID_ARG;
+  moe::wait_probe_kernel<<<1, 64, 0, moe::as_stream(stream)>>>(static_cast<int*>(ws), limit_ns);
+  return moe::launch_status();
+}
 
 extern "C" moe_status_t moe_read_probe(const void* src, size_t bytes, float* sink, void* stream) {
   if (!src || !sink || bytes % 16 != 0 || !moe::aligned16(src)) return MOE_ERR_INVALID_ARG;

@@ -66,7 +66,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // the CTA's abort flag is (or becomes) set, or if the wait ran out of time (in
 // which case this call sets the abort flag). The clock and the flag are looked
 // at once every 256 polls, so a wait that succeeds soon costs only the polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              uint64_t limit_ns) {
   uint64_t t0 = 0;
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -75,12 +76,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       const uint64_t now = globaltimer();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitLimitNs) {
+      } else if (now - t0 > limit_ns) {
         *abort_flag = 1;
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_wait_for(bar, parity, abort_flag, kWaitLimitNs);
 }
 
 // Same wait with cluster-scope acquire: for barriers that receive arrivals from
