@@ -403,7 +403,55 @@ def bench_decode(moe, synth, torch, dev, flush, peaks, args):
         out[f"T{T}"] = {"ms": round(ms, 4), "active_experts": n_active, "weight_bytes": wbytes,
                         "GB/s": round(gbs, 1), "frac_hbm": round(gbs / float(peaks["hbm_gbs"]), 4),
                         "tokens/s": round(T / (ms * 1e-3), 1)}
+    # the same layers with FP8-e4m3 weights (per-channel scales, made on the device by torch's e4m3
+    # cast) through moe_fused_forward_fp8: one byte per weight streamed
+    def dev_quant(w, chunk=16):
+        E_, R_, K_ = w.shape
+        q = torch.empty((E_, R_, K_), dtype=torch.uint8, device=w.device)
+        sc = torch.empty((E_, R_), dtype=torch.float32, device=w.device)
+        for e0 in range(0, E_, chunk):
+            w32 = w[e0:e0 + chunk].float()
+            amax = w32.abs().amax(dim=2)
+            s_ = amax / torch.full_like(amax, 448.0)
+            s_ = torch.where(s_ == 0, torch.ones_like(s_), s_)
+            q[e0:e0 + chunk] = (w32 / s_[:, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+            sc[e0:e0 + chunk] = s_
+            del w32
+        return q, sc
+    q1, s1 = dev_quant(W["w1"])
+    q2, s2 = dev_quant(W["w2"])
     del W
+    torch.cuda.empty_cache()
+    fp8 = {}
+    for T in (1, 8, 32, 128):
+        cfg = synth.decode_config(T)
+        acts = synth.moe_activations(cfg, dev)
+        ws = torch.zeros(moe.moe_fused_forward_fp8_workspace_size(T, cfg.H, cfg.I, cfg.E, cfg.topk),
+                         dtype=torch.uint8, device=dev)
+        run = lambda: moe.moe_fused_forward_fp8(acts["x"], acts["gating"], q1, s1, q2, s2, cfg.topk,
+                                                cfg.renormalize, cfg.num_expert_group, cfg.topk_group, cfg.scoring,
+                                                cfg.routed_scaling_factor, ws=ws)
+        for _ in range(3):
+            _, _, ids = run()
+        torch.cuda.synchronize()
+        n_active = int(np.unique(ids.cpu().numpy()).size)
+        times = []
+        for k in range(max(5, args.steps)):
+            flush(k)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            run()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        wbytes = n_active * 3 * cfg.I * cfg.H
+        gbs = wbytes / (ms * 1e-3) / 1e9
+        fp8[f"T{T}"] = {"ms": round(ms, 4), "active_experts": n_active, "weight_bytes": wbytes,
+                        "GB/s": round(gbs, 1), "frac_hbm": round(gbs / float(peaks["hbm_gbs"]), 4),
+                        "tokens/s": round(T / (ms * 1e-3), 1)}
+    out["fp8_e4m3"] = fp8
+    del q1, q2, s1, s2
     torch.cuda.empty_cache()
     return out
 

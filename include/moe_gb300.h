@@ -200,8 +200,10 @@ MOE_API moe_status_t moe_fused_forward(const void* x, const float* gating, const
  *  scales_down      [E, H] fp32 per-output-channel scales (16-byte aligned).
  *  Other arguments, outputs and conditions as for moe_fused_forward (H a multiple of
  *  256, I a multiple of 128); ws of at least moe_fused_forward_fp8_workspace_size(...)
- *  bytes, 256-byte aligned and zero-filled before its first use. Every problem size
- *  uses the 128-row block layout (no decode-specific kernel for this dtype).
+ *  bytes, 256-byte aligned and zero-filled before its first use. Kernels as for
+ *  moe_fused_forward: decode-sized problems (T * topk <= 32 * E) take the swap-AB
+ *  kernels (128 weight rows on the MMA's M side, an expert's tokens on N, 16-row
+ *  blocks), streaming one byte per weight; larger ones the 128-row block layout.
  *  Streams: x is quantised on a second stream of the library's own (one per host
  *  thread and device, created at the first call and kept), forked from `stream` by an
  *  event at the start of the call and joined back into it before the gate_up GEMM,

@@ -54,6 +54,13 @@ moe_status_t launch_gemm_down_fp8(const uint8_t* qh, const float* sh, const uint
 moe_status_t launch_quant_rows_e4m3_bf16(const __nv_bfloat16* x, int M, int K, uint8_t* q, float* s,
                                          const int* rows_dev, cudaStream_t st);
 
+moe_status_t launch_swap_gate_up_fp8(const uint8_t* qx, const float* sx, const uint8_t* w1, const float* sw1,
+                                     const int32_t* sorted_ids, const int32_t* offsets, __nv_bfloat16* h, int* err,
+                                     int num_pairs, int topk, int H, int I, int E, cudaStream_t s);
+moe_status_t launch_swap_down_fp8(const uint8_t* qh, const float* sh, const uint8_t* w2, const float* sw2,
+                                  const int32_t* sorted_ids, const int32_t* offsets, const float* topk_w,
+                                  float* y_acc, int* err, int num_pairs, int topk, int cap, int H, int I, int E,
+                                  cudaStream_t s);
 moe_status_t launch_swap_gate_up(const __nv_bfloat16* x, const __nv_bfloat16* w1, const int32_t* sorted_ids,
                                  const int32_t* offsets, __nv_bfloat16* h, int* err, int num_pairs, int topk, int H,
                                  int I, int E, int nmax, cudaStream_t s);
@@ -127,9 +134,9 @@ FusedLayout fused_layout(int T, int H, int I, int E, int topk, int block_m) {
   return L;
 }
 
-// The FP8 forward's workspace: the bf16 forward's 128-row layout, then the
-// per-token e4m3 codes of x and their scales, then the per-row e4m3 codes of h
-// and their scales.
+// The FP8 forward's workspace: the bf16 forward's layout for the selected kernels, then
+// the per-token e4m3 codes of x and their scales, then the per-row e4m3 codes of h and
+// their scales.
 struct Fp8Layout {
   FusedLayout base;
   size_t qx, sx, qh, sh, total;
@@ -137,7 +144,7 @@ struct Fp8Layout {
 
 Fp8Layout fp8_layout(int T, int H, int I, int E, int topk) {
   Fp8Layout L{};
-  L.base = fused_layout(T, H, I, E, topk, 128);
+  L.base = fused_layout(T, H, I, E, topk, choose_plan(T, E, topk).block_m);
   size_t off = align_up(L.base.total, 1024);
   L.qx = off; off = align_up(off + static_cast<size_t>(T) * H, 1024);
   L.sx = off; off = align_up(off + static_cast<size_t>(T) * 4, 1024);
@@ -352,6 +359,7 @@ extern "C" moe_status_t moe_fused_forward_fp8(const void* x, const float* gating
   float* sh = reinterpret_cast<float*>(w + L.sh);
   const int num_pairs = T * topk;
   const int cap = L.base.cap;
+  const Plan plan = choose_plan(T, E, topk);
 
   stage_mark(0, s);
   // x's per-token codes depend on x alone: quantised on the side stream while routing
@@ -364,9 +372,10 @@ extern "C" moe_status_t moe_fused_forward_fp8(const void* x, const float* gating
     if (st != MOE_OK) return st;
     if (cudaEventRecord(side->join, side->st) != cudaSuccess) return MOE_ERR_CUDA;
   }
+  // decode-sized problems: the swap-AB kernels, whose accumulator rows the routing kernel clears
   st = route_and_align(gating, T, E, num_expert_group, topk_group, topk, scoring, renormalize, routed_scaling_factor,
-                       topk_weights, topk_ids, nullptr, H, 128, sorted_ids, expert_ids, offsets, ntpp,
-                       w + L.base.align_scratch, err, sorted_tok, tile_counter, s);
+                       topk_weights, topk_ids, plan.swap ? y_acc : nullptr, H, plan.block_m, sorted_ids, expert_ids,
+                       offsets, ntpp, w + L.base.align_scratch, err, sorted_tok, tile_counter, s);
   if (st != MOE_OK) return st;
   stage_mark(2, s);
   if (side) {
@@ -376,15 +385,23 @@ extern "C" moe_status_t moe_fused_forward_fp8(const void* x, const float* gating
     if (st != MOE_OK) return st;
   }
   stage_mark(3, s);
-  st = launch_gemm_gate_up_pairs_fp8(qx, sx, static_cast<const uint8_t*>(w_gate_up), scales_gate_up, sorted_tok,
-                                     offsets, h, err, H, I, E, y_acc, static_cast<size_t>(T) * H, tile_counter, s);
+  if (plan.swap)
+    st = launch_swap_gate_up_fp8(qx, sx, static_cast<const uint8_t*>(w_gate_up), scales_gate_up, sorted_ids, offsets,
+                                 h, err, num_pairs, topk, H, I, E, s);
+  else
+    st = launch_gemm_gate_up_pairs_fp8(qx, sx, static_cast<const uint8_t*>(w_gate_up), scales_gate_up, sorted_tok,
+                                       offsets, h, err, H, I, E, y_acc, static_cast<size_t>(T) * H, tile_counter, s);
   if (st != MOE_OK) return st;
   stage_mark(4, s);
   st = launch_quant_rows_e4m3_bf16(h, cap, I, qh, sh, ntpp, s);
   if (st != MOE_OK) return st;
   stage_mark(5, s);
-  st = launch_gemm_down_fp8(qh, sh, static_cast<const uint8_t*>(w_down), scales_down, sorted_ids, expert_ids, ntpp,
-                            topk_weights, y_acc, err, num_pairs, topk, cap, H, I, E, s);
+  if (plan.swap)
+    st = launch_swap_down_fp8(qh, sh, static_cast<const uint8_t*>(w_down), scales_down, sorted_ids, offsets,
+                              topk_weights, y_acc, err, num_pairs, topk, cap, H, I, E, s);
+  else
+    st = launch_gemm_down_fp8(qh, sh, static_cast<const uint8_t*>(w_down), scales_down, sorted_ids, expert_ids,
+                              ntpp, topk_weights, y_acc, err, num_pairs, topk, cap, H, I, E, s);
   if (st != MOE_OK) return st;
   stage_mark(6, s);
   const size_t n4 = static_cast<size_t>(T) * H / 4;

@@ -424,6 +424,21 @@ bool make_tmap_u8_2d_k64(CUtensorMap* map, const void* base, uint64_t rows, uint
   return r == CUDA_SUCCESS;
 }
 
+// 2D 8-bit tensor map over a row-major [rows, cols] byte matrix, box = 128 bytes x box_rows rows,
+// 128B swizzle (tcgen05 operand).
+bool make_tmap_u8_2d_k128_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, int box_rows) {
+  auto encode = get_encode_fn();
+  if (!encode || box_rows < 1 || box_rows > 256) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2D 8-bit tensor map over a row-major [rows, cols] byte matrix, box = 128 x 128,
 // 128B swizzle (tcgen05 operand) or none (staging read back by threads).
 bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, bool swizzle128) {

@@ -16,6 +16,14 @@
 //   down:    D0/D1 = W2[e][h0 .. h0+256) h_tok^T,
 //            y_acc[token(pos), h0 + i] += w(pos) * D[i, pos]
 //
+// The kernels are written in bytes of K: a K step is one 128-byte row segment of
+// both operands, 64 bf16 or 128 FP8-e4m3 values, four MMAs of 32 bytes of K each
+// (kind::f16 K=16 or kind::f8f6f4 K=32). The FP8 instance (the low-precision GMM
+// article's layer: per-token activation scales, per-channel weight scales, fp32
+// accumulation) gathers the per-token codes of x, scales each gate_up accumulator by
+// its token's and its channel's scale before the SwiGLU, and folds h's per-row scale
+// into the route weight and the down channel scale into the combine.
+//
 // One CTA per SM, persistent. Warps 0-3 epilogue (TMEM lane = weight row),
 // warps 4..3+S producers (gate_up: warp 4+s owns ring slot s: lane 0 sends the
 // two weight tiles by TMA, the warp gathers the token rows with cp.async; down:
@@ -30,18 +38,19 @@
 namespace moe {
 
 bool make_tmap_bf16_2d_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, int box_rows);
+bool make_tmap_u8_2d_k128_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, int box_rows);
 
 namespace {
 
-constexpr int kSwBK = 64;
+constexpr int kSwKB = 128;  // bytes of K per step: one 128-byte swizzle row (64 bf16 or 128 e4m3)
 constexpr int kSwM = 128;
-constexpr int kSwATile = kSwM * kSwBK * 2;  // 16 KB
+constexpr int kSwATile = kSwM * kSwKB;  // 16 KB
 
 enum SwapMode { kSwGateUp = 0, kSwDown = 1 };
 
 template <int NMAX>
 struct SwapCfg {
-  static constexpr int kBBytes = NMAX * kSwBK * 2;
+  static constexpr int kBBytes = NMAX * kSwKB;
   static constexpr int kStageBytes = 2 * kSwATile + kBBytes;
   static constexpr int kStages = (196608 / kStageBytes) > 6 ? 6 : (196608 / kStageBytes);
   static constexpr int kProdWarps = kStages;
@@ -50,19 +59,22 @@ struct SwapCfg {
   static constexpr int kBufs = NMAX <= 128 ? 2 : 1;
   static constexpr int kD1Off = NMAX <= 128 ? 128 : 256;  // TMEM column offset of D1 within a buffer
   static constexpr int kStagingBytes = 32 * kSwM * 2;      // gate_up epilogue transpose tile [32 tok][128] bf16
-  static constexpr int kCtlBytes = 512 + 4 * (MOE_MAX_EXPERTS + 1) + kProdWarps * NMAX * 4 + 2 * NMAX * 4;
+  static constexpr int kCtlBytes = 512 + 4 * (MOE_MAX_EXPERTS + 1) + kProdWarps * NMAX * 4 + 3 * NMAX * 4;
   static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes + kStagingBytes + kCtlBytes;
 };
 
 struct SwapArgs {
-  const __nv_bfloat16* x;      // gate_up: [T, H]
+  const uint8_t* x;            // gate_up: [T, H] bf16 or e4m3 codes (bytes)
+  const float* sx;             // FP8 gate_up: per-token scales of x [T]
+  const float* sa;             // FP8 down: per-row scales of h [cap]
+  const float* sw;             // FP8: per-channel weight scales [E, a_rows_per_expert]
   const int32_t* sorted_ids;   // [cap] (16-row blocks)
   const int32_t* offsets;      // [E + 1] padded segment starts (multiples of 16)
   const float* topk_w;         // down: [num_pairs]
   __nv_bfloat16* h;            // gate_up out: [cap, I]
   float* y_acc;                // down out: [T, H]
   int* err;
-  int num_pairs, topk, E, K, I, H;
+  int num_pairs, topk, E, K, I, H;  // K: reduction length in bytes
   int n_wb;                    // weight blocks per expert
   int a_rows_per_expert;       // 2I or H
   int a1_offset;               // row offset of the second weight tile (I for gate_up, 128 for down)
@@ -103,7 +115,7 @@ __device__ __forceinline__ SwapTile decode_swap(const int* pfx, const SwapArgs& 
   return st;
 }
 
-template <int MODE, int NMAX>
+template <int MODE, int NMAX, bool F8>
 __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
     moe_swap_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_b,
                     const SwapArgs args) {
@@ -127,6 +139,7 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
   int* rowtabs = pfx + (MOE_MAX_EXPERTS + 1);                                     // [kProdWarps][NMAX]
   int* tok_s = rowtabs + C::kProdWarps * NMAX;                                    // [NMAX] epilogue token
   float* w_s = reinterpret_cast<float*>(tok_s + NMAX);                            // [NMAX] epilogue weight
+  float* sx_s = w_s + NMAX;                                                       // [NMAX] FP8: token scales
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -185,7 +198,7 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int tasks = pfx[args.E];
-  const int kblocks = args.K / kSwBK;
+  const int kblocks = args.K / kSwKB;
 
   if (warp >= 4 && warp < C::kMmaWarp) {
     // ------------------------------------------------------------ producers
@@ -222,11 +235,12 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
         if (lane == 0) {
           const int wrow = st.e * args.a_rows_per_expert + st.wb * args.wb_stride;
           ptx::mbar_arrive_expect_tx(full_bar(slot), 2 * kSwATile);
-          ptx::tma_load_2d(a_dst, &map_w, full_bar(slot), kb * kSwBK, wrow);
-          ptx::tma_load_2d(a_dst + kSwATile, &map_w, full_bar(slot), kb * kSwBK, wrow + args.a1_offset);
+          ptx::tma_load_2d(a_dst, &map_w, full_bar(slot), kb * kSwKB / (F8 ? 1 : 2), wrow);
+          ptx::tma_load_2d(a_dst + kSwATile, &map_w, full_bar(slot), kb * kSwKB / (F8 ? 1 : 2),
+                           wrow + args.a1_offset);
           ++fills;
         }
-        const int k0 = kb * kSwBK + chunk * 8;
+        const int k0 = kb * kSwKB + chunk * 16;  // bytes
         for (int r = rsub; r < st.n; r += 4) {
           const int off = rowtab[r];
           const uint32_t dst = b_dst + r * 128 + ((chunk ^ (r & 7)) << 4);
@@ -251,9 +265,10 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t a_dst = sbase + stage * C::kStageBytes;
           ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * kSwATile + C::kBBytes);
-          ptx::tma_load_2d(a_dst, &map_w, full_bar(stage), kb * kSwBK, wrow);
-          ptx::tma_load_2d(a_dst + kSwATile, &map_w, full_bar(stage), kb * kSwBK, wrow + args.a1_offset);
-          ptx::tma_load_2d(a_dst + 2 * kSwATile, &map_b, full_bar(stage), kb * kSwBK, st.row0);
+          const int kc = kb * kSwKB / (F8 ? 1 : 2);  // K coordinate in elements
+          ptx::tma_load_2d(a_dst, &map_w, full_bar(stage), kc, wrow);
+          ptx::tma_load_2d(a_dst + kSwATile, &map_w, full_bar(stage), kc, wrow + args.a1_offset);
+          ptx::tma_load_2d(a_dst + 2 * kSwATile, &map_b, full_bar(stage), kc, st.row0);
           ++fills[stage];
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
@@ -270,7 +285,7 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < tasks && ok; t += gridDim.x, ++it) {
         const SwapTile st = decode_swap<NMAX>(pfx, args, t);
-        const uint32_t idesc = ptx::idesc_bf16_f32(kSwM, st.n);
+        const uint32_t idesc = F8 ? ptx::idesc_e4m3_f32(kSwM, st.n) : ptx::idesc_bf16_f32(kSwM, st.n);
         const int b = C::kBufs == 2 ? (it & 1) : 0;
         const uint32_t tph = C::kBufs == 2 ? ((it >> 1) & 1) : (it & 1);
         if (!ptx::mbar_wait(tempty_bar(b), tph ^ 1u, abort_flag)) break;
@@ -283,9 +298,14 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
           const uint64_t a0 = ptx::sdesc_sw128(s0), a1 = ptx::sdesc_sw128(s0 + kSwATile);
           const uint64_t bd = ptx::sdesc_sw128(s0 + 2 * kSwATile);
 #pragma unroll
-          for (int kk = 0; kk < kSwBK / 16; ++kk) {
-            ptx::mma_f16(d0, a0 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
-            ptx::mma_f16(d1, a1 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < kSwKB / 32; ++kk) {  // 32 bytes of K per MMA
+            if constexpr (F8) {
+              ptx::mma_f8(d0, a0 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+              ptx::mma_f8(d1, a1 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+            } else {
+              ptx::mma_f16(d0, a0 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+              ptx::mma_f16(d1, a1 + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+            }
           }
           ptx::mma_commit(empty_bar(stage));
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -305,16 +325,30 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
       const SwapTile st = decode_swap<NMAX>(pfx, args, t);
       const int b = C::kBufs == 2 ? (it & 1) : 0;
       const uint32_t tph = C::kBufs == 2 ? ((it >> 1) & 1) : (it & 1);
-      // per-tile token table (token index, route weight) for the down epilogue
-      if (MODE == kSwDown) {
+      // per-tile token table (token index, route weight) for the down epilogue; FP8: the
+      // route weight times h's row scale (down), the token scales of x (gate_up)
+      if (MODE == kSwDown || F8) {
         asm volatile("bar.sync 1, 128;" ::: "memory");
         for (int j = i; j < st.n; j += 128) {
           const int sid = __ldg(args.sorted_ids + st.row0 + j);
           const bool valid = sid < args.num_pairs;
-          tok_s[j] = valid ? sid / args.topk : -1;
-          w_s[j] = valid ? __ldg(args.topk_w + sid) : 0.f;
+          if (MODE == kSwDown) {
+            tok_s[j] = valid ? sid / args.topk : -1;
+            float w = valid ? __ldg(args.topk_w + sid) : 0.f;
+            if (F8) w *= valid ? __ldg(args.sa + st.row0 + j) : 0.f;
+            w_s[j] = w;
+          } else {
+            sx_s[j] = valid ? __ldg(args.sx + sid / args.topk) : 0.f;
+          }
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
+      }
+      // FP8: this lane's two channel scales (rows i and a1_offset + i of the weight block)
+      float cs0 = 1.f, cs1 = 1.f;
+      if (F8) {
+        const float* sw = args.sw + static_cast<size_t>(st.e) * args.a_rows_per_expert + st.wb * args.wb_stride;
+        cs0 = __ldg(sw + i);
+        cs1 = __ldg(sw + args.a1_offset + i);
       }
       if (!ptx::mbar_wait(tfull_bar(b), tph, abort_flag)) break;
       ptx::tc_fence_after();
@@ -329,8 +363,14 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
           // h[row0 + c*32 + j, n0 + i] for j < jn, transposed through [32 tok][128] bf16
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float g = __uint_as_float(v0[j]);
-            hstage[j * kSwM + i] = __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(v1[j]));
+            float g = __uint_as_float(v0[j]), u = __uint_as_float(v1[j]);
+            if (F8) {
+              // g = sx[token] * sw[e, n] * acc_g, u = sx[token] * sw[e, I + n] * acc_u
+              const float rs = sx_s[c * 32 + j];
+              g = rs * cs0 * g;
+              u = rs * cs1 * u;
+            }
+            hstage[j * kSwM + i] = __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * u);
           }
           asm volatile("bar.sync 1, 128;" ::: "memory");
           // 16 lanes store one token's 256 bytes: a warp covers 2 tokens per instruction
@@ -350,8 +390,13 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
             if (j < jn && tok >= 0) {
               const float w = w_s[c * 32 + j];
               float* yrow = args.y_acc + static_cast<size_t>(tok) * args.H + h0;
-              atomicAdd(yrow + i, w * __uint_as_float(v0[j]));
-              atomicAdd(yrow + kSwM + i, w * __uint_as_float(v1[j]));
+              if (F8) {  // w * sh[row] (folded in w_s) * sw[e, channel] * acc
+                atomicAdd(yrow + i, (w * cs0) * __uint_as_float(v0[j]));
+                atomicAdd(yrow + kSwM + i, (w * cs1) * __uint_as_float(v1[j]));
+              } else {
+                atomicAdd(yrow + i, w * __uint_as_float(v0[j]));
+                atomicAdd(yrow + kSwM + i, w * __uint_as_float(v1[j]));
+              }
             }
           }
         }
@@ -368,12 +413,12 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
   if (tid == 0 && *abort_flag) report_error(args.err, MOE_DEVERR_TIMEOUT);
 }
 
-template <int MODE, int NMAX>
+template <int MODE, int NMAX, bool F8>
 moe_status_t launch_swap_impl(const CUtensorMap& mw, const CUtensorMap& mb, const SwapArgs& a, cudaStream_t s) {
   using C = SwapCfg<NMAX>;
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_swap_kernel<MODE, NMAX>), static_cast<int>(C::kSmem)))
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_swap_kernel<MODE, NMAX, F8>), static_cast<int>(C::kSmem)))
     return MOE_ERR_CUDA;
-  moe_swap_kernel<MODE, NMAX><<<num_sms(), C::kThreads, C::kSmem, s>>>(mw, mb, a);
+  moe_swap_kernel<MODE, NMAX, F8><<<num_sms(), C::kThreads, C::kSmem, s>>>(mw, mb, a);
   return launch_status();
 }
 
@@ -386,11 +431,11 @@ moe_status_t launch_swap_gate_up(const __nv_bfloat16* x, const __nv_bfloat16* w1
   CUtensorMap mw;
   if (!make_tmap_bf16_2d_rows(&mw, w1, static_cast<uint64_t>(E) * 2 * I, H, kSwM)) return MOE_ERR_CUDA;
   SwapArgs a{};
-  a.x = x; a.sorted_ids = sorted_ids; a.offsets = offsets; a.h = h; a.err = err;
-  a.num_pairs = num_pairs; a.topk = topk; a.E = E; a.K = H; a.I = I; a.H = H;
+  a.x = reinterpret_cast<const uint8_t*>(x); a.sorted_ids = sorted_ids; a.offsets = offsets; a.h = h; a.err = err;
+  a.num_pairs = num_pairs; a.topk = topk; a.E = E; a.K = 2 * H; a.I = I; a.H = H;
   a.n_wb = I / kSwM; a.a_rows_per_expert = 2 * I; a.a1_offset = I; a.wb_stride = kSwM;
-  if (nmax <= 32) return launch_swap_impl<kSwGateUp, 32>(mw, mw, a, s);
-  return launch_swap_impl<kSwGateUp, 256>(mw, mw, a, s);
+  if (nmax <= 32) return launch_swap_impl<kSwGateUp, 32, false>(mw, mw, a, s);
+  return launch_swap_impl<kSwGateUp, 256, false>(mw, mw, a, s);
 }
 
 moe_status_t launch_swap_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, const int32_t* sorted_ids,
@@ -402,10 +447,39 @@ moe_status_t launch_swap_down(const __nv_bfloat16* h, const __nv_bfloat16* w2, c
   if (!make_tmap_bf16_2d_rows(&mb, h, static_cast<uint64_t>(cap), I, box)) return MOE_ERR_CUDA;
   SwapArgs a{};
   a.sorted_ids = sorted_ids; a.offsets = offsets; a.topk_w = topk_w; a.y_acc = y_acc; a.err = err;
-  a.num_pairs = num_pairs; a.topk = topk; a.E = E; a.K = I; a.I = I; a.H = H;
+  a.num_pairs = num_pairs; a.topk = topk; a.E = E; a.K = 2 * I; a.I = I; a.H = H;
   a.n_wb = H / (2 * kSwM); a.a_rows_per_expert = H; a.a1_offset = kSwM; a.wb_stride = 2 * kSwM;
-  if (nmax <= 32) return launch_swap_impl<kSwDown, 32>(mw, mb, a, s);
-  return launch_swap_impl<kSwDown, 256>(mw, mb, a, s);
+  if (nmax <= 32) return launch_swap_impl<kSwDown, 32, false>(mw, mb, a, s);
+  return launch_swap_impl<kSwDown, 256, false>(mw, mb, a, s);
+}
+
+// FP8-e4m3 operands (decode-sized problems: token tiles of <= 32). qx: per-token codes
+// of x [T, H] with scales sx [T]; w1: codes [E, 2I, H] with per-channel scales sw1 [E, 2I].
+moe_status_t launch_swap_gate_up_fp8(const uint8_t* qx, const float* sx, const uint8_t* w1, const float* sw1,
+                                     const int32_t* sorted_ids, const int32_t* offsets, __nv_bfloat16* h, int* err,
+                                     int num_pairs, int topk, int H, int I, int E, cudaStream_t s) {
+  CUtensorMap mw;
+  if (!make_tmap_u8_2d_k128_rows(&mw, w1, static_cast<uint64_t>(E) * 2 * I, H, kSwM)) return MOE_ERR_CUDA;
+  SwapArgs a{};
+  a.x = qx; a.sx = sx; a.sw = sw1; a.sorted_ids = sorted_ids; a.offsets = offsets; a.h = h; a.err = err;
+  a.num_pairs = num_pairs; a.topk = topk; a.E = E; a.K = H; a.I = I; a.H = H;
+  a.n_wb = I / kSwM; a.a_rows_per_expert = 2 * I; a.a1_offset = I; a.wb_stride = kSwM;
+  return launch_swap_impl<kSwGateUp, 32, true>(mw, mw, a, s);
+}
+
+// qh: per-row codes of h [cap, I] with scales sh [cap]; w2: codes [E, H, I] with sw2 [E, H].
+moe_status_t launch_swap_down_fp8(const uint8_t* qh, const float* sh, const uint8_t* w2, const float* sw2,
+                                  const int32_t* sorted_ids, const int32_t* offsets, const float* topk_w,
+                                  float* y_acc, int* err, int num_pairs, int topk, int cap, int H, int I, int E,
+                                  cudaStream_t s) {
+  CUtensorMap mw, mb;
+  if (!make_tmap_u8_2d_k128_rows(&mw, w2, static_cast<uint64_t>(E) * H, I, kSwM)) return MOE_ERR_CUDA;
+  if (!make_tmap_u8_2d_k128_rows(&mb, qh, static_cast<uint64_t>(cap), I, 32)) return MOE_ERR_CUDA;
+  SwapArgs a{};
+  a.sa = sh; a.sw = sw2; a.sorted_ids = sorted_ids; a.offsets = offsets; a.topk_w = topk_w; a.y_acc = y_acc;
+  a.err = err; a.num_pairs = num_pairs; a.topk = topk; a.E = E; a.K = I; a.I = I; a.H = H;
+  a.n_wb = H / (2 * kSwM); a.a_rows_per_expert = H; a.a1_offset = kSwM; a.wb_stride = 2 * kSwM;
+  return launch_swap_impl<kSwDown, 32, true>(mw, mb, a, s);
 }
 
 }  // namespace moe
