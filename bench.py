@@ -405,21 +405,8 @@ def bench_decode(moe, synth, torch, dev, flush, peaks, args):
                         "tokens/s": round(T / (ms * 1e-3), 1)}
     # the same layers with FP8-e4m3 weights (per-channel scales, made on the device by torch's e4m3
     # cast) through moe_fused_forward_fp8: one byte per weight streamed
-    def dev_quant(w, chunk=16):
-        E_, R_, K_ = w.shape
-        q = torch.empty((E_, R_, K_), dtype=torch.uint8, device=w.device)
-        sc = torch.empty((E_, R_), dtype=torch.float32, device=w.device)
-        for e0 in range(0, E_, chunk):
-            w32 = w[e0:e0 + chunk].float()
-            amax = w32.abs().amax(dim=2)
-            s_ = amax / torch.full_like(amax, 448.0)
-            s_ = torch.where(s_ == 0, torch.ones_like(s_), s_)
-            q[e0:e0 + chunk] = (w32 / s_[:, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
-            sc[e0:e0 + chunk] = s_
-            del w32
-        return q, sc
-    q1, s1 = dev_quant(W["w1"])
-    q2, s2 = dev_quant(W["w2"])
+    q1, s1 = device_e4m3_weights(torch, W["w1"])
+    q2, s2 = device_e4m3_weights(torch, W["w2"])
     del W
     torch.cuda.empty_cache()
     fp8 = {}
@@ -736,6 +723,89 @@ def run_reference(args, rank, world, cfg=None, n: int = 256):
     }
 
 
+def device_e4m3_weights(torch, w, chunk=16):
+    """Per-output-channel e4m3 codes of bf16 weights [E, R, K] made on the device: torch's float8_e4m3fn
+    cast (nearest, ties to even) of w / (absmax / 448) in fp32, a few experts at a time."""
+    E_, R_, K_ = w.shape
+    q = torch.empty((E_, R_, K_), dtype=torch.uint8, device=w.device)
+    sc = torch.empty((E_, R_), dtype=torch.float32, device=w.device)
+    for e0 in range(0, E_, chunk):
+        w32 = w[e0:e0 + chunk].float()
+        amax = w32.abs().amax(dim=2)
+        s_ = amax / torch.full_like(amax, 448.0)
+        s_ = torch.where(s_ == 0, torch.ones_like(s_), s_)
+        q[e0:e0 + chunk] = (w32 / s_[:, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+        sc[e0:e0 + chunk] = s_
+        del w32
+    return q, sc
+
+
+def profile_case(name: str) -> None:
+    """Small, fixed workloads for ncu captures (each runs a few calls and exits; the profile
+    summaries under profiles/ name the case and the ncu command).
+
+    decode_small  decode-shaped layer with 32 experts (H=7168, I=2048, T=32, top-8 grouped
+                  sigmoid; 2.8 GB of bf16 weights, more than L2), bf16 then FP8, twice each
+    lowp          gmm_lowp on the C5 and small-K workloads, INT8 then e4m3
+    route         grouped top-k at T=65536 (E=256, G=8/4, top-8) and of the prefill layer
+    layers        prefill layer (bf16, then FP8) 3 calls each; decode T=32 (E=256) bf16 and FP8
+    """
+    import torch
+    import mixture_experts_routing_grouped_gb300 as moe
+    import synth
+    from mixture_experts_routing_grouped_gb300 import build as _b
+    _b.build()
+    dev = "cuda"
+    if name == "decode_small":
+        cfg = synth.MoEConfig("decode_T32_H7168_I2048_E32_top8", T=32, H=7168, I=2048, E=32, topk=8,
+                              num_expert_group=8, topk_group=4, scoring="sigmoid", routed_scaling_factor=2.5,
+                              logit_sigma=2.0, seed=41)
+        acts, W = synth.moe_activations(cfg, dev), synth.moe_weights(cfg, dev)
+        q1, s1 = device_e4m3_weights(torch, W["w1"])
+        q2, s2 = device_e4m3_weights(torch, W["w2"])
+        for _ in range(2):
+            moe.moe_fused_forward(acts["x"], acts["gating"], W["w1"], W["w2"], 8, True, 8, 4, "sigmoid", 2.5)
+            moe.moe_fused_forward_fp8(acts["x"], acts["gating"], q1, s1, q2, s2, 8, True, 8, 4, "sigmoid", 2.5)
+    elif name == "lowp":
+        for cfg in (synth.lowp_config(), synth.lowp_small_k_config()):
+            d = synth.gmm_inputs(cfg, dev)
+            for qdt in (torch.int8, torch.float8_e4m3fn):
+                qx, sx = moe.moe_quant_per_token(d["x"], qdt)
+                qw, sw = moe.moe_quant_per_token(d["w"].view(cfg.E * cfg.N, cfg.K), qdt)
+                moe.gmm_lowp(qx, qw.view(cfg.E, cfg.N, cfg.K), sx, sw.view(cfg.E, cfg.N), d["expert_offsets"],
+                             d["expert_sizes"])
+    elif name == "route":
+        cfg = synth.routing_config(65536, "sigmoid")
+        moe.moe_grouped_topk(synth.gating_logits(cfg, dev), 8, True, 8, 4, "sigmoid", 2.5)
+        cfg = synth.prefill_config()
+        moe.moe_grouped_topk(synth.gating_logits(cfg, dev), 8, True, 1, 1, "softmax", 1.0)
+    elif name == "layers":
+        cfg = synth.prefill_config()
+        acts, W = synth.moe_activations(cfg, dev), synth.moe_weights(cfg, dev)
+        q1, s1 = device_e4m3_weights(torch, W["w1"])
+        q2, s2 = device_e4m3_weights(torch, W["w2"])
+        for _ in range(3):
+            moe.moe_fused_forward(acts["x"], acts["gating"], W["w1"], W["w2"], 8, True)
+        for _ in range(3):
+            moe.moe_fused_forward_fp8(acts["x"], acts["gating"], q1, s1, q2, s2, 8, True)
+        del W, q1, q2
+        torch.cuda.empty_cache()
+        cfg = synth.decode_config(32)
+        acts, W = synth.moe_activations(cfg, dev), synth.moe_weights(cfg, dev)
+        for _ in range(2):
+            moe.moe_fused_forward(acts["x"], acts["gating"], W["w1"], W["w2"], 8, True, 8, 4, "sigmoid", 2.5)
+        q1, s1 = device_e4m3_weights(torch, W["w1"])
+        q2, s2 = device_e4m3_weights(torch, W["w2"])
+        del W
+        torch.cuda.empty_cache()
+        for _ in range(2):
+            moe.moe_fused_forward_fp8(acts["x"], acts["gating"], q1, s1, q2, s2, 8, True, 8, 4, "sigmoid", 2.5)
+    else:
+        raise ValueError(f"unknown profile case {name!r}")
+    torch.cuda.synchronize()
+    print(f"profile case {name}: ok", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -746,9 +816,14 @@ def main():
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["routing", "decode", "lowp", "fp8"],
                     help="run just one sub-benchmark on one GPU and print its JSON (profiling cases)")
+    ap.add_argument("--profile-case", choices=["decode_small", "lowp", "route", "layers"],
+                    help="run one small fixed workload for an ncu capture and exit (no timing)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local_rank = dist_env()
+    if args.profile_case:
+        profile_case(args.profile_case)
+        return
 
     if args.impl == "reference":
         if rank != 0:
