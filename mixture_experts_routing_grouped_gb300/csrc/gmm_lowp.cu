@@ -22,7 +22,8 @@
 // Kernel shape (one persistent CTA per SM): warps 0-3 epilogue, warp 4 task
 // claimer + TMA producer (FP8: both operands; INT8: weight codes), warp 5
 // owner of TMEM + MMA issuer, INT8 only: warps 6-13 weight converters, warp 14
-// TMA producer of the widened activations. Tile 128 rows x 128 columns x 128 K; a task is
+// TMA producer of the widened activations; then four more epilogue warps (the
+// first four drain columns 0-63 of each accumulator row, these 64-127). Tile 128 rows x 128 columns x 128 K; a task is
 // (expert, 128-row block, 128-column block), ordered expert, column block, row
 // block so that CTAs running together share each weight tile in L2. Rows of a
 // block past the expert's end are computed on whatever TMA brought (the next
@@ -55,10 +56,13 @@ constexpr int kQ = 4;                                   // task queue slots
 constexpr int kLTmemCols = 2 * kLBN;
 constexpr int kF8Ring = kF8Stages * 2 * kTile8;         // 192 KB
 constexpr int kI8Ring = kI8OpOff + kI8Ops * kTile16;    // 224 KB
-constexpr size_t kLSmem = 1024 + kI8Ring + 512;
+constexpr size_t kLSmem = 1024 + kI8Ring + 512 + 2 * kLBN * 4;
 static_assert(kLSmem <= 232448, "shared memory per CTA");
 template <bool I8>
-constexpr int lowp_threads() { return 32 * (I8 ? kI8AWarp + 1 : 6); }
+constexpr int lowp_threads() { return 32 * ((I8 ? kI8AWarp + 1 : 6) + 4); }  // + 4 more epilogue warps
+// The second half of the epilogue: four warps after the kernel's other roles.
+template <bool I8>
+constexpr int lowp_epi2_warp0() { return I8 ? kI8AWarp + 1 : 6; }
 
 struct LowpArgs {
   const float* sx;
@@ -206,13 +210,15 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
   volatile int* tq = reinterpret_cast<volatile int*>(ctl + 384);       // [kQ] claimed task ids
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 400);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 404);
+  float* scl = reinterpret_cast<float*>(ctl + 512);                    // [2][kLBN] epilogue channel scales
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = args.N / kLBN;
   const int kblocks = args.K / kLBK;
   const int num_tasks = __ldg(args.num_tasks);
   constexpr int kConvThreads = I8 ? 32 * kI8ConvWarps : 0;
-  constexpr int kConsumers = 1 + 128 + kConvThreads + (I8 ? 1 : 0);
+  constexpr int kConsumers = 1 + 256 + kConvThreads + (I8 ? 1 : 0);
+  constexpr int kEpi2 = lowp_epi2_warp0<I8>();
 
   if (tid == 0) {
     for (int s = 0; s < 8; ++s) {
@@ -231,7 +237,7 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(tfull_bar(b), 1);
-      ptx::mbar_init(tempty_bar(b), 128);
+      ptx::mbar_init(tempty_bar(b), 256);
     }
     ptx::mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -336,7 +342,7 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       }
     }
     __syncwarp();
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < kEpi2) {
     // ------------------------------------------------------------ int8 -> fp16 weight converters
     if constexpr (I8) {
       const int c = tid - 192;  // 0 .. kConvThreads-1
@@ -433,34 +439,47 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ epilogue (warps 0-3)
-    const int r = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // ------------------------------------------------------------ epilogue (warps 0-3 and kEpi2..kEpi2+3)
+    // Two warps per TMEM lane quarter, each draining half of the tile's columns. The tile's 128
+    // channel scales are copied to shared memory (one per thread of the first four warps, double
+    // buffered by accumulator) before the wait for the accumulator, so that no global load sits
+    // between a TMEM chunk and its stores; each chunk's TMEM load is issued before the previous
+    // chunk is scaled and stored.
+    const bool second = warp >= kEpi2;
+    const int quarter = warp & 3;  // a warp reaches only TMEM lanes [32 * (warp % 4), +32)
+    const int c0 = second ? kLBN / 64 : 0;  // first 32-column chunk of this warp (two chunks each)
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     for (int it = 0;; ++it) {
       const int t = next_task(it);
       if (t < 0 || t >= num_tasks) break;
       const Task k = decode_task(args, n_tiles, t);
       const int b = it & 1;
-      if (!ptx::mbar_wait(tfull_bar(b), (it >> 1) & 1, abort_flag)) break;
-      ptx::tc_fence_after();
+      float* sc = scl + b * kLBN;
+      if (!second) sc[r] = __ldg(args.sw + static_cast<size_t>(k.e) * args.N + k.nt * kLBN + r);
       const bool valid = r < k.rows;
       const int row = k.row0 + r;
       const float sx = valid ? __ldg(args.sx + row) : 0.f;
-      const float* swp = args.sw + static_cast<size_t>(k.e) * args.N + k.nt * kLBN;
-#pragma unroll 1
-      for (int cc = 0; cc < kLBN / 32; ++cc) {
-        uint32_t d[32];
-        ptx::tmem_ld32(tmem_base + lane_off + b * kLBN + cc * 32, d);
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight epilogue warps: scales staged
+      if (!ptx::mbar_wait(tfull_bar(b), (it >> 1) & 1, abort_flag)) break;
+      ptx::tc_fence_after();
+      uint32_t d[2][32];
+      ptx::tmem_ld32(tmem_base + lane_off + b * kLBN + c0 * 32, d[0]);
+#pragma unroll
+      for (int ci = 0; ci < kLBN / 64; ++ci) {
+        const int cc = c0 + ci;
         ptx::tmem_ld_wait();
+        if (ci + 1 < kLBN / 64) ptx::tmem_ld32(tmem_base + lane_off + b * kLBN + (cc + 1) * 32, d[(ci + 1) & 1]);
         if (valid) {
+          const uint32_t* dc = d[ci & 1];
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
-            const float4 s4 = __ldg(reinterpret_cast<const float4*>(swp + cc * 32 + j));
-            v[j] = sx * s4.x * __uint_as_float(d[j]);
-            v[j + 1] = sx * s4.y * __uint_as_float(d[j + 1]);
-            v[j + 2] = sx * s4.z * __uint_as_float(d[j + 2]);
-            v[j + 3] = sx * s4.w * __uint_as_float(d[j + 3]);
+            const float4 s4 = *reinterpret_cast<const float4*>(sc + cc * 32 + j);
+            v[j] = sx * s4.x * __uint_as_float(dc[j]);
+            v[j + 1] = sx * s4.y * __uint_as_float(dc[j + 1]);
+            v[j + 2] = sx * s4.z * __uint_as_float(dc[j + 2]);
+            v[j + 3] = sx * s4.w * __uint_as_float(dc[j + 3]);
           }
           const size_t o = static_cast<size_t>(row) * args.N + k.nt * kLBN + cc * 32;
           if (args.out_f32) {
