@@ -14,20 +14,27 @@
 // (exact for |q| <= 128) and the MMA is kind::f16 with fp32 accumulation: the
 // activation codes once, by a pre-pass into the workspace (every row block is
 // reused by all N / 128 column blocks, so widening it per tile repeated the work
-// N / 128 times and bounded the kernel), the weight codes per tile in shared
-// memory by eight converter warps, after TMA brought them in unconverted. The
-// weight codes (the HBM stream), the widened activations (L2-resident) and the
-// widened weights move through separate rings.
+// N / 128 times and bounded the kernel), the weight codes per tile by eight
+// converter warps, which read the codes TMA brought into shared memory and
+// write the fp16 values straight into tensor memory. The MMA takes the widened
+// weights as its A operand from tensor memory and the widened activations as
+// its B operand from shared memory, so the product is transposed (accumulator
+// lane = output channel, column = token) and its token count N is the task's
+// row count rounded up to 16: an expert with 60 rows costs a 128 x 64 MMA, and
+// only the 32-row slabs holding its rows are loaded. Staging the widened
+// weights through shared memory instead cost the MMA a second 32 KB operand
+// read and the converters a 32 KB write per K step, and shared-memory
+// bandwidth bounded the kernel.
 //
 // Kernel shape (one persistent CTA per SM): warps 0-3 epilogue, warp 4 task
 // claimer + TMA producer (FP8: both operands; INT8: weight codes), warp 5
 // owner of TMEM + MMA issuer, INT8 only: warps 6-13 weight converters, warp 14
 // TMA producer of the widened activations; then four more epilogue warps (the
-// first four drain columns 0-63 of each accumulator row, these 64-127). Tile 128 rows x 128 columns x 128 K; a task is
-// (expert, 128-row block, 128-column block), ordered expert, column block, row
-// block so that CTAs running together share each weight tile in L2. Rows of a
-// block past the expert's end are computed on whatever TMA brought (the next
-// expert's rows or zero fill) and never stored.
+// first four drain accumulator columns 0-63, these 64-127). Tile 128 rows x
+// 128 columns x 128 K; a task is (expert, 128-row block, 128-column block),
+// ordered expert, column block, row block so that CTAs running together share
+// each weight tile in L2. Rows of a block past the expert's end are computed on
+// whatever TMA brought (the next expert's rows or zero fill) and never stored.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -37,7 +44,7 @@
 namespace moe {
 
 bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, bool swizzle128);
-bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols);
+bool make_tmap_bf16_2d_rows(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, int box_rows);
 
 namespace {
 
@@ -45,17 +52,20 @@ constexpr int kLBM = 128, kLBN = 128, kLBK = 128;      // K in elements (= bytes
 constexpr int kTile8 = kLBM * kLBK;                     // 16 KB: one 8-bit operand tile
 constexpr int kF8Stages = 6;                            // fp8: 6 x (A 16 KB + B 16 KB)
 constexpr int kTile16 = kLBM * kLBK * 2;                // 32 KB: one fp16 operand tile (2 column blocks)
-constexpr int kI8BStages = 4;                           // int8: 4 x 16 KB weight codes
-constexpr int kI8AStages = 3;                           // int8: 3 x 32 KB widened activations
-constexpr int kI8Ops = 2;                               // int8: 2 x 32 KB widened weight tiles
+constexpr int kI8BStages = 6;                           // int8: 6 x 16 KB weight codes
+constexpr int kI8AStages = 4;                           // int8: 4 x 32 KB widened activations
+constexpr int kI8Ops = 4;                               // int8: widened weight tiles in TMEM, 64 columns each
 constexpr int kI8ConvWarps = 8;
 constexpr int kI8AWarp = 6 + kI8ConvWarps;              // warp 14: activation producer
 constexpr int kI8AOff = kI8BStages * kTile8;
-constexpr int kI8OpOff = kI8AOff + kI8AStages * kTile16;
+constexpr int kI8Slab = 32;                             // int8: activation rows per TMA load
 constexpr int kQ = 4;                                   // task queue slots
-constexpr int kLTmemCols = 2 * kLBN;
+constexpr int kI8OpCol = 2 * kLBN;                      // int8: first TMEM column of the weight tiles
+template <bool I8>
+constexpr int lowp_tmem_cols() { return I8 ? 512 : 2 * kLBN; }  // accumulators (+ int8 weight tiles)
+static_assert(kI8OpCol + kI8Ops * kLBK / 2 <= 512, "tensor memory columns");
 constexpr int kF8Ring = kF8Stages * 2 * kTile8;         // 192 KB
-constexpr int kI8Ring = kI8OpOff + kI8Ops * kTile16;    // 224 KB
+constexpr int kI8Ring = kI8AOff + kI8AStages * kTile16; // 224 KB
 constexpr size_t kLSmem = 1024 + kI8Ring + 512 + 2 * kLBN * 4;
 static_assert(kLSmem <= 232448, "shared memory per CTA");
 template <bool I8>
@@ -191,15 +201,16 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
   const uint32_t sbase = raw_addr + pad;
   constexpr int kStages = I8 ? kI8BStages : kF8Stages;
   // fp8: stage s = [A 16 KB | B 16 KB] at s*32 KB.
-  // int8: weight-code stage s (16 KB, unswizzled) at s*16 KB; widened activations
-  //       a (32 KB: 2 column blocks of [128 rows][128 B], 128B swizzle) after the
-  //       code ring; widened weight operand o (32 KB, same layout) after those.
+  // int8: weight-code stage s (16 KB: [128 rows][128 B], 128B swizzle) at s*16 KB;
+  //       widened activations a (32 KB: 2 column blocks of [128 rows][128 B],
+  //       128B swizzle) after the code ring. Widened weight tile o sits in TMEM
+  //       columns [kI8OpCol + 64 o, +64): lane = channel, two K values a column.
   uint8_t* ctl = smem + (I8 ? kI8Ring : kF8Ring);
   const uint32_t bar0 = ptx::smem_u32(ctl);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };                 // staging / stage landed
   auto empty_bar = [&](int s) { return bar0 + 8u * (8 + s); };          // staging / stage free
-  auto ofull_bar = [&](int s) { return bar0 + 8u * (16 + s); };         // int8: fp16 operand ready
-  auto oempty_bar = [&](int s) { return bar0 + 8u * (20 + s); };        // int8: fp16 operand free
+  auto ofull_bar = [&](int s) { return bar0 + 8u * (16 + s); };         // int8: fp16 weight tile ready
+  auto oempty_bar = [&](int s) { return bar0 + 8u * (20 + s); };        // int8: fp16 weight tile free
   auto tfull_bar = [&](int b) { return bar0 + 8u * (24 + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (26 + b); };
   auto qfull_bar = [&](int q) { return bar0 + 8u * (28 + q); };
@@ -210,7 +221,7 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
   volatile int* tq = reinterpret_cast<volatile int*>(ctl + 384);       // [kQ] claimed task ids
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 400);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 404);
-  float* scl = reinterpret_cast<float*>(ctl + 512);                    // [2][kLBN] epilogue channel scales
+  float* scl = reinterpret_cast<float*>(ctl + 512);  // [2][128] epilogue scales: fp8 channel, int8 token
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = args.N / kLBN;
@@ -244,7 +255,7 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
     ptx::fence_mbar_init();
   }
   if (warp == 5) {
-    ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(tmem_slot)), kLTmemCols);
+    ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(tmem_slot)), lowp_tmem_cols<I8>());
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -325,12 +336,17 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
         const int t = next_task(it);
         if (t < 0 || t >= num_tasks) break;
         const Task k = decode_task(args, n_tiles, t);
+        const int slabs = (k.rows + kI8Slab - 1) / kI8Slab;  // only the 32-row slabs holding the task's rows
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait(aempty_bar(astage), aphase ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t dst = sbase + kI8AOff + astage * kTile16;
-          ptx::mbar_arrive_expect_tx(afull_bar(astage), kTile16);
-          ptx::tma_load_2d(dst, &map_x, afull_bar(astage), kb * kLBK, k.row0);
-          ptx::tma_load_2d(dst + kTile8, &map_x, afull_bar(astage), kb * kLBK + kLBK / 2, k.row0);
+          ptx::mbar_arrive_expect_tx(afull_bar(astage), slabs * kI8Slab * 128 * 2);
+          for (int j = 0; j < slabs; ++j) {
+            const uint32_t o = j * kI8Slab * 128;
+            ptx::tma_load_2d(dst + o, &map_x, afull_bar(astage), kb * kLBK, k.row0 + j * kI8Slab);
+            ptx::tma_load_2d(dst + kTile8 + o, &map_x, afull_bar(astage), kb * kLBK + kLBK / 2,
+                             k.row0 + j * kI8Slab);
+          }
           ++issued;
           if (++astage == kI8AStages) { astage = 0; aphase ^= 1u; }
         }
@@ -345,7 +361,15 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
   } else if (warp >= 6 && warp < kEpi2) {
     // ------------------------------------------------------------ int8 -> fp16 weight converters
     if constexpr (I8) {
-      const int c = tid - 192;  // 0 .. kConvThreads-1
+      // Thread = one weight row (channel r, the TMEM lane this warp may write) and one half
+      // of the K step: codes [64 half, +64) of row r, four 16-byte chunks of the swizzled
+      // stage (chunk j of row r sits at chunk j ^ (r & 7), so a warp's loads spread over all
+      // banks), widened to 32 words of fp16 pairs and stored to TMEM columns [32 half, +32)
+      // of the weight tile.
+      const int quarter = warp & 3;
+      const int half = (warp - 6) >> 2;
+      const int r = quarter * 32 + lane;
+      const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
       int stage = 0, ostage = 0;
       uint32_t phase = 0, ophase = 0;
       bool ok = true;
@@ -354,34 +378,26 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
         if (t < 0 || t >= num_tasks) break;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
-          if (!ptx::mbar_wait(oempty_bar(ostage), ophase ^ 1u, abort_flag)) { ok = false; break; }
-          const uint8_t* src = smem + stage * kTile8;
-          const uint32_t dst = sbase + kI8OpOff + ostage * kTile16;
-          // 128 rows x 8 chunks of 16 codes; thread c takes chunk (c & 7) of rows c/8 + (kConvThreads/8) i
+          const uint8_t* src = smem + stage * kTile8 + r * 128;
+          uint4 v[4];
 #pragma unroll
-          for (int i = 0; i < 1024 / kConvThreads; ++i) {
-            const int r = (c >> 3) + (kConvThreads / 8) * i;
-            const int ch = c & 7;  // codes k in [ch*16, ch*16+16)
-            const uint4 v = *reinterpret_cast<const uint4*>(src + r * 128 + ch * 16);
-            uint32_t h[8];
-            i8x4_to_f16x4(v.x, h[0], h[1]);
-            i8x4_to_f16x4(v.y, h[2], h[3]);
-            i8x4_to_f16x4(v.z, h[4], h[5]);
-            i8x4_to_f16x4(v.w, h[6], h[7]);
-            // fp16 k index ch*16 .. +16 -> column block cb = ch / 4, 16-byte chunks j0, j0+1 in the 128-byte row
-            const int cb = ch >> 2;
-            const int j0 = (ch & 3) * 2;
-            const uint32_t rowbase = dst + cb * kTile8 + r * 128;
-            const uint32_t d0 = rowbase + (((j0) ^ (r & 7)) << 4);
-            const uint32_t d1 = rowbase + (((j0 + 1) ^ (r & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d0), "r"(h[0]), "r"(h[1]), "r"(h[2]),
-                         "r"(h[3]) : "memory");
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(d1), "r"(h[4]), "r"(h[5]), "r"(h[6]),
-                         "r"(h[7]) : "memory");
+          for (int q = 0; q < 4; ++q)
+            v[q] = *reinterpret_cast<const uint4*>(src + ((((half << 2) + q) ^ (r & 7)) << 4));
+          uint32_t h[32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            i8x4_to_f16x4(v[q].x, h[8 * q + 0], h[8 * q + 1]);
+            i8x4_to_f16x4(v[q].y, h[8 * q + 2], h[8 * q + 3]);
+            i8x4_to_f16x4(v[q].z, h[8 * q + 4], h[8 * q + 5]);
+            i8x4_to_f16x4(v[q].w, h[8 * q + 6], h[8 * q + 7]);
           }
-          ptx::fence_proxy_async_smem();
-          ptx::mbar_arrive(ofull_bar(ostage));
           ptx::mbar_arrive(empty_bar(stage));
+          if (!ptx::mbar_wait(oempty_bar(ostage), ophase ^ 1u, abort_flag)) { ok = false; break; }
+          ptx::tc_fence_after();
+          ptx::tmem_st32(tmem_base + lane_off + kI8OpCol + ostage * (kLBK / 2) + half * 32, h);
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(ofull_bar(ostage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
           if (++ostage == kI8Ops) { ostage = 0; ophase ^= 1u; }
         }
@@ -398,6 +414,11 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       for (int it = 0; ok; ++it) {
         const int t = next_task(it);
         if (t < 0 || t >= num_tasks) break;
+        uint32_t idesc_t = idesc;
+        if constexpr (I8) {  // transposed product: N = the task's tokens, rounded up to 16
+          const int n_tok = (decode_task(args, n_tiles, t).rows + 15) & ~15;
+          idesc_t = (idesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(n_tok >> 3) << 17);
+        }
         const int b = it & 1;
         if (!ptx::mbar_wait(tempty_bar(b), ((it >> 1) & 1) ^ 1u, abort_flag)) break;
         ptx::tc_fence_after();
@@ -410,12 +431,12 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
               break;
             }
             ptx::tc_fence_after();
-            const uint32_t a = sbase + kI8AOff + astage * kTile16;
-            const uint32_t bop = sbase + kI8OpOff + ostage * kTile16;
+            const uint32_t act = sbase + kI8AOff + astage * kTile16;
+            const uint32_t wt = tmem_base + kI8OpCol + ostage * (kLBK / 2);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 0; kk < 8; ++kk) {  // K 16 kk .. +16: 8 TMEM columns, 32 bytes of a 128-byte row
               const uint32_t off = (kk >> 2) * kTile8 + (kk & 3) * 32;
-              ptx::mma_f16(d_tmem, ptx::sdesc_sw128(a + off), ptx::sdesc_sw128(bop + off), idesc, (kb | kk) != 0);
+              ptx::mma_f16_ts(d_tmem, wt + 8 * kk, ptx::sdesc_sw128(act + off), idesc_t, (kb | kk) != 0);
             }
             ptx::mma_commit(oempty_bar(ostage));
             ptx::mma_commit(aempty_bar(astage));
@@ -440,8 +461,9 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-3 and kEpi2..kEpi2+3)
-    // Two warps per TMEM lane quarter, each draining half of the tile's columns. The tile's 128
-    // channel scales are copied to shared memory (one per thread of the first four warps, double
+    // Two warps per TMEM lane quarter, each draining half of the tile's columns. The scales that
+    // vary along the columns (fp8: the tile's 128 channel scales; int8, transposed: its tokens'
+    // scales) are copied to shared memory (one per thread of the first four warps, double
     // buffered by accumulator) before the wait for the accumulator, so that no global load sits
     // between a TMEM chunk and its stores; each chunk's TMEM load is issued before the previous
     // chunk is scaled and stored.
@@ -450,6 +472,49 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
     const int c0 = second ? kLBN / 64 : 0;  // first 32-column chunk of this warp (two chunks each)
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    if constexpr (I8) {
+      // Lane r holds output channel nt * 128 + r; column m holds the task's token m. A warp's
+      // store for one token writes 32 consecutive channels of its output row.
+      for (int it = 0;; ++it) {
+        const int t = next_task(it);
+        if (t < 0 || t >= num_tasks) break;
+        const Task k = decode_task(args, n_tiles, t);
+        const int b = it & 1;
+        float* sc = scl + b * kLBN;
+        if (!second) sc[r] = r < k.rows ? __ldg(args.sx + k.row0 + r) : 0.f;
+        const float sw = __ldg(args.sw + static_cast<size_t>(k.e) * args.N + k.nt * kLBN + r);
+        const int chunks = min(kLBN / 64, max(0, (k.rows - c0 * 32 + 31) / 32));  // warp-uniform
+        asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight epilogue warps: scales staged
+        if (!ptx::mbar_wait(tfull_bar(b), (it >> 1) & 1, abort_flag)) break;
+        ptx::tc_fence_after();
+        uint32_t d[2][32];
+        if (chunks > 0) ptx::tmem_ld32(tmem_base + lane_off + b * kLBN + c0 * 32, d[0]);
+#pragma unroll
+        for (int ci = 0; ci < kLBN / 64; ++ci) {
+          if (ci >= chunks) break;
+          const int cc = c0 + ci;
+          ptx::tmem_ld_wait();
+          if (ci + 1 < chunks) ptx::tmem_ld32(tmem_base + lane_off + b * kLBN + (cc + 1) * 32, d[(ci + 1) & 1]);
+          const uint32_t* dc = d[ci & 1];
+          const int m_end = min(32, k.rows - cc * 32);
+          const size_t o = static_cast<size_t>(k.row0 + cc * 32) * args.N + k.nt * kLBN + r;
+          if (args.out_f32) {
+            float* dst = static_cast<float*>(args.out) + o;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < m_end) dst[static_cast<size_t>(j) * args.N] = sc[cc * 32 + j] * sw * __uint_as_float(dc[j]);
+          } else {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.out) + o;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < m_end)
+                dst[static_cast<size_t>(j) * args.N] = __float2bfloat16_rn(sc[cc * 32 + j] * sw * __uint_as_float(dc[j]));
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(tempty_bar(b));
+      }
+    } else {
     for (int it = 0;; ++it) {
       const int t = next_task(it);
       if (t < 0 || t >= num_tasks) break;
@@ -498,12 +563,13 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty_bar(b));
     }
+    }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (warp == 5) ptx::tmem_dealloc(tmem_base, kLTmemCols);
+  if (warp == 5) ptx::tmem_dealloc(tmem_base, lowp_tmem_cols<I8>());
   if (tid == 0 && *abort_flag) report_error(args.err, MOE_DEVERR_TIMEOUT);
 }
 
@@ -560,11 +626,11 @@ extern "C" moe_status_t gmm_lowp(const void* input, const void* weights, const f
     const int grid = static_cast<int>(std::min<size_t>((n16 + 255) / 256, static_cast<size_t>(num_sms()) * 8));
     widen_i8_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(input), static_cast<uint4*>(xh), n16);
     if ((st = launch_status()) != MOE_OK) return st;
-    if (!make_tmap_bf16_2d(&map_x, xh, M, K)) return MOE_ERR_CUDA;
+    if (!make_tmap_bf16_2d_rows(&map_x, xh, M, K, kI8Slab)) return MOE_ERR_CUDA;
   } else if (!make_tmap_u8_2d(&map_x, input, M, K, true)) {
     return MOE_ERR_CUDA;
   }
-  if (!make_tmap_u8_2d(&map_w, weights, static_cast<uint64_t>(E) * N, K, !i8)) return MOE_ERR_CUDA;
+  if (!make_tmap_u8_2d(&map_w, weights, static_cast<uint64_t>(E) * N, K, true)) return MOE_ERR_CUDA;
   LowpArgs a{};
   a.sx = scales_x; a.sw = scales_w; a.offsets = expert_offsets; a.sizes = expert_sizes; a.mt_prefix = mt_prefix;
   a.counter = counter; a.num_tasks = num_tasks; a.out = out; a.err = err;
