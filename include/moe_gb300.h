@@ -312,7 +312,12 @@ MOE_API moe_status_t moe_quant_per_token(const void* x, int x_dt, int M, int K, 
  *                 any expert are left untouched.
  *  K multiple of 128, N multiple of 128. Inconsistent metadata: the offending
  *  expert is skipped and MOE_DEVERR_GROUP_META is set.
- *  ws, ws_bytes   at least gmm_lowp_workspace_size(...) bytes.
+ *  ws, ws_bytes   at least gmm_lowp_workspace_size(...) bytes, 256-byte aligned,
+ *                 zero-filled before its first use: bytes [4, 12) hold the task
+ *                 counters, which every call leaves zero for the next one (one call at
+ *                 a time per workspace); ws[0..4) is the error word.
+ *  One launch for e4m3 (the GEMM, started as a programmatic dependent of the kernel
+ *  before it in the stream), two for INT8 (the activation widening, then the GEMM).
  */
 MOE_API size_t gmm_lowp_workspace_size(int M, int K, int N, int E);
 MOE_API moe_status_t gmm_lowp(const void* input, const void* weights, const float* scales_x,

@@ -26,11 +26,12 @@
 // read and the converters a 32 KB write per K step, and shared-memory
 // bandwidth bounded the kernel.
 //
-// Kernel shape (one persistent CTA per SM): warps 0-3 epilogue, warp 4 task
-// claimer + TMA producer (FP8: both operands; INT8: weight codes), warp 5
+// Kernel shape (one persistent CTA per SM): warps 0-3 epilogue, warp 4 TMA
+// producer (FP8: both operands; INT8: weight codes), warp 5
 // owner of TMEM + MMA issuer, INT8 only: warps 6-13 weight converters, warp 14
 // TMA producer of the widened activations; then four more epilogue warps (the
-// first four drain accumulator columns 0-63, these 64-127). Tile 128 rows x
+// first four drain accumulator columns 0-63, these 64-127) and the task
+// scheduler, which claims and decodes tasks for the others. Tile 128 rows x
 // 128 columns x 128 K; a task is (expert, 128-row block, 128-column block),
 // ordered expert, column block, row block so that CTAs running together share
 // each weight tile in L2. Rows of a block past the expert's end are computed on
@@ -66,96 +67,37 @@ constexpr int lowp_tmem_cols() { return I8 ? 512 : 2 * kLBN; }  // accumulators 
 static_assert(kI8OpCol + kI8Ops * kLBK / 2 <= 512, "tensor memory columns");
 constexpr int kF8Ring = kF8Stages * 2 * kTile8;         // 192 KB
 constexpr int kI8Ring = kI8AOff + kI8AStages * kTile16; // 224 KB
-constexpr size_t kLSmem = 1024 + kI8Ring + 512 + 2 * kLBN * 4;
+constexpr size_t kLSmem = 1024 + kI8Ring + 512 + 2 * kLBN * 4 + kQ * 16;
 static_assert(kLSmem <= 232448, "shared memory per CTA");
 template <bool I8>
-constexpr int lowp_threads() { return 32 * ((I8 ? kI8AWarp + 1 : 6) + 4); }  // + 4 more epilogue warps
+constexpr int lowp_threads() { return 32 * ((I8 ? kI8AWarp + 1 : 6) + 5); }  // + 4 more epilogue warps + scheduler
 // The second half of the epilogue: four warps after the kernel's other roles.
 template <bool I8>
 constexpr int lowp_epi2_warp0() { return I8 ? kI8AWarp + 1 : 6; }
+// The task scheduler: the last warp.
+template <bool I8>
+constexpr int lowp_sched_warp() { return lowp_epi2_warp0<I8>() + 4; }
 
 struct LowpArgs {
   const float* sx;
   const float* sw;
   const int32_t* offsets;
   const int32_t* sizes;
-  const int32_t* mt_prefix;  // [E+1] row blocks before each expert
-  int* counter;              // task counter (zeroed by the prep kernel)
-  const int* num_tasks;
+  int* counter;              // tasks claimed beyond the first gridDim.x (zero at launch)
+  int* exit_ticket;          // CTAs finished (zero at launch); the last one re-zeroes both
   void* out;
   int* err;
   int M, K, N, E, out_f32;
 };
 
+// A task: expert e's 128-row block starting at row0 (rows of them real) times column
+// block nt. Task ids run expert by expert; within an expert, column block by column
+// block, row blocks fastest, so that CTAs running together share each weight tile in
+// L2. Expert e's tasks are [P[e] * n_tiles, P[e+1] * n_tiles), P the prefix sum of the
+// experts' row-block counts (experts with inconsistent metadata count zero blocks).
 struct Task {
   int e, row0, rows, nt;
 };
-
-// Task t -> (expert, row block, column block). Tasks of one expert are laid out
-// column block by column block, row blocks fastest.
-__device__ __forceinline__ Task decode_task(const LowpArgs& a, int n_tiles, int t) {
-  const int g_tile_task = t;  // tasks before expert e = prefix[e] * n_tiles
-  int lo = 0, hi = a.E;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(a.mt_prefix + mid) * n_tiles <= g_tile_task) lo = mid; else hi = mid;
-  }
-  while (lo + 1 < a.E && __ldg(a.mt_prefix + lo + 1) * n_tiles <= g_tile_task) ++lo;
-  Task k;
-  k.e = lo;
-  const int mcount = __ldg(a.mt_prefix + lo + 1) - __ldg(a.mt_prefix + lo);
-  const int local = t - __ldg(a.mt_prefix + lo) * n_tiles;
-  k.nt = local / mcount;
-  const int mt = local - k.nt * mcount;
-  const int off = __ldg(a.offsets + lo);
-  const int size = __ldg(a.sizes + lo);
-  k.row0 = off + mt * kLBM;
-  k.rows = min(kLBM, off + size - k.row0);
-  return k;
-}
-
-// Validates the group metadata, counts 128-row blocks per expert and zeroes the task counter.
-__global__ void __launch_bounds__(1024) lowp_prep_kernel(const int32_t* __restrict__ offsets,
-                                                         const int32_t* __restrict__ sizes, int E, int M,
-                                                         int n_tiles, int32_t* __restrict__ mt_prefix,
-                                                         int* __restrict__ counter, int* __restrict__ num_tasks,
-                                                         int* __restrict__ err) {
-  __shared__ int warp_tot[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int blocks = 0;
-  if (tid < E) {
-    const int o0 = offsets[tid], o1 = offsets[tid + 1], s = sizes[tid];
-    const bool ok = s >= 0 && o0 >= 0 && o1 <= M && o1 - o0 == s;
-    if (!ok) report_error(err, MOE_DEVERR_GROUP_META);
-    else blocks = (s + kLBM - 1) / kLBM;
-  }
-  if (tid == 0 && (offsets[0] != 0 || offsets[E] != M)) report_error(err, MOE_DEVERR_GROUP_META);
-  int incl = blocks;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int t = warp_tot[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += n;
-    }
-    warp_tot[lane] = t;
-  }
-  __syncthreads();
-  const int excl = incl - blocks + (warp > 0 ? warp_tot[warp - 1] : 0);
-  if (tid < E) mt_prefix[tid] = excl;
-  if (tid == E - 1) {
-    mt_prefix[E] = excl + blocks;
-    *num_tasks = (excl + blocks) * n_tiles;
-  }
-  if (tid == 0) *counter = 0;
-}
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -218,17 +160,17 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
   const uint32_t done_bar = bar0 + 8u * 36;
   auto afull_bar = [&](int s) { return bar0 + 8u * (37 + s); };         // int8: activations landed
   auto aempty_bar = [&](int s) { return bar0 + 8u * (41 + s); };        // int8: activations free
-  volatile int* tq = reinterpret_cast<volatile int*>(ctl + 384);       // [kQ] claimed task ids
+  auto taken_bar = [&](int q) { return bar0 + 8u * (45 + q); };         // queue entry taken by the TMA thread
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 400);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 404);
   float* scl = reinterpret_cast<float*>(ctl + 512);  // [2][128] epilogue scales: fp8 channel, int8 token
+  volatile int* tq = reinterpret_cast<volatile int*>(ctl + 512 + 2 * kLBN * 4);  // [kQ][4] claimed tasks
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = args.N / kLBN;
   const int kblocks = args.K / kLBK;
-  const int num_tasks = __ldg(args.num_tasks);
   constexpr int kConvThreads = I8 ? 32 * kI8ConvWarps : 0;
-  constexpr int kConsumers = 1 + 256 + kConvThreads + (I8 ? 1 : 0);
+  constexpr int kConsumers = 1 + 1 + 256 + kConvThreads + (I8 ? 1 : 0);  // TMA, MMA, epilogue, int8 roles
   constexpr int kEpi2 = lowp_epi2_warp0<I8>();
 
   if (tid == 0) {
@@ -246,6 +188,7 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       ptx::mbar_init(qfull_bar(s), 1);
       ptx::mbar_init(qempty_bar(s), kConsumers);
     }
+    for (int q = 0; q < kQ; ++q) ptx::mbar_init(taken_bar(q), 1);
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(tfull_bar(b), 1);
       ptx::mbar_init(tempty_bar(b), 256);
@@ -262,47 +205,119 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched as a programmatic dependent of the kernel before it in the stream (for
+  // INT8 the activation widening): the prologue above overlapped that kernel; nothing
+  // in global memory is read or written before it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // Task queue consumer: returns the next task id (>= num_tasks means done) or -1 on abort.
-  auto next_task = [&](int it) -> int {
+  // Task queue consumer: the claiming thread decodes every task once and publishes
+  // it whole, so that no consumer waits on the dependent global loads of a decode.
+  // Returns false when the tasks are done (expert -1) or on abort.
+  auto next_task = [&](int it, Task& k) -> bool {
     const int q = it % kQ;
-    if (!ptx::mbar_wait(qfull_bar(q), (static_cast<uint32_t>(it / kQ) & 1u), abort_flag)) return -1;
-    const int t = tq[q];
+    if (!ptx::mbar_wait(qfull_bar(q), (static_cast<uint32_t>(it / kQ) & 1u), abort_flag)) return false;
+    k.e = tq[4 * q];
+    k.row0 = tq[4 * q + 1];
+    k.rows = tq[4 * q + 2];
+    k.nt = tq[4 * q + 3];
     ptx::mbar_arrive(qempty_bar(q));
-    return t;
+    return k.e >= 0;
   };
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ task claimer + TMA producer
+  if (warp == lowp_sched_warp<I8>()) {
+    // ------------------------------------------------------------ task scheduler
+    // The CTA's first task is blockIdx.x; every further one is claimed from the global
+    // counter (an L2 round trip) once the TMA thread has taken the previous one, so a
+    // CTA holds at most one task beyond the one it is loading and the claims stay
+    // balanced to the end. The whole warp decodes: it walks the experts 32 at a time
+    // (lane l holds expert c0 + l's offset, size, 128-row block count and the
+    // inclusive prefix of the counts), which it can do forwards only because a CTA's
+    // claims increase. Experts whose metadata do not add up count zero blocks and set
+    // MOE_DEVERR_GROUP_META (every CTA walks every expert by the time the tasks run out).
+    // Claiming and decoding in the TMA thread stalled its loads at every task boundary
+    // by a chain of dependent global loads; with small K a task is only a few K steps
+    // (the article's small-K case, section 4.2, interleaves two experts per block
+    // against the same gap).
+    int c0 = 0, base = 0;  // first expert of the chunk, row blocks before it
+    int o_l = 0, s_l = 0, nb_l = 0, incl_l = 0, total = 0;
+    auto load_chunk = [&]() {
+      const int e = c0 + lane;
+      o_l = 0; s_l = 0; nb_l = 0;
+      if (e < args.E) {
+        o_l = __ldg(args.offsets + e);
+        const int o1 = __ldg(args.offsets + e + 1);
+        s_l = __ldg(args.sizes + e);
+        if (s_l >= 0 && o_l >= 0 && o1 <= args.M && o1 - o_l == s_l) nb_l = (s_l + kLBM - 1) / kLBM;
+        else report_error(args.err, MOE_DEVERR_GROUP_META);
+      }
+      incl_l = nb_l;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl_l, o);
+        if (lane >= o) incl_l += v;
+      }
+      total = __shfl_sync(0xffffffffu, incl_l, 31);
+    };
+    if (blockIdx.x == 0 && lane == 0 &&
+        (__ldg(args.offsets) != 0 || __ldg(args.offsets + args.E) != args.M))
+      report_error(args.err, MOE_DEVERR_GROUP_META);
+    load_chunk();
+    for (int it = 0;; ++it) {
+      if (it > 0 && !ptx::mbar_wait(taken_bar((it - 1) % kQ), static_cast<uint32_t>((it - 1) / kQ) & 1u,
+                                    abort_flag))
+        break;
+      int t = static_cast<int>(blockIdx.x);
+      if (it > 0 && lane == 0) t = static_cast<int>(gridDim.x) + atomicAdd(args.counter, 1);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      const int mb = t / n_tiles;  // expert e holds the task iff P[e] <= mb < P[e + 1]
+      Task k;
+      k.e = -1; k.row0 = 0; k.rows = 0; k.nt = 0;
+      while (c0 < args.E) {
+        const unsigned m = __ballot_sync(0xffffffffu, c0 + lane < args.E && base + incl_l > mb);
+        if (m != 0u) {
+          const int l = __ffs(m) - 1;
+          const int pe = base + __shfl_sync(0xffffffffu, incl_l - nb_l, l);
+          const int mcount = __shfl_sync(0xffffffffu, nb_l, l);
+          const int off = __shfl_sync(0xffffffffu, o_l, l);
+          const int size = __shfl_sync(0xffffffffu, s_l, l);
+          const int local = t - pe * n_tiles;
+          k.e = c0 + l;
+          k.nt = local / mcount;
+          k.row0 = off + (local - k.nt * mcount) * kLBM;
+          k.rows = min(kLBM, off + size - k.row0);
+          break;
+        }
+        base += total;
+        c0 += 32;
+        load_chunk();
+      }
+      if (lane == 0) {
+        const int q = it % kQ;
+        if (ptx::mbar_wait(qempty_bar(q), (static_cast<uint32_t>(it / kQ) & 1u) ^ 1u, abort_flag)) {
+          tq[4 * q] = k.e;
+          tq[4 * q + 1] = k.row0;
+          tq[4 * q + 2] = k.rows;
+          tq[4 * q + 3] = k.nt;
+          ptx::mbar_arrive(qfull_bar(q));
+        } else {
+          k.e = -1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, k.e, 0) < 0) break;
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
-      // The next task is claimed (an L2 round trip) and published three K steps
-      // before the current task's last load, so that its loads follow the current
-      // ones without a gap: with small K a task is only a few K steps, and a
-      // claim at the task boundary left the ring empty for a claim's latency every
-      // task (the article's small-K case, section 4.2, interleaves two experts per
-      // block for the same reason).
-      auto publish = [&](int it, int t) -> bool {
-        const int q = it % kQ;
-        if (!ptx::mbar_wait(qempty_bar(q), (static_cast<uint32_t>(it / kQ) & 1u) ^ 1u, abort_flag)) return false;
-        tq[q] = t;
-        ptx::mbar_arrive(qfull_bar(q));
-        return true;
-      };
-      const int claim_at = kblocks > 3 ? kblocks - 3 : 0;
-      int t = atomicAdd(args.counter, 1);
-      bool ok = publish(0, t);
-      for (int it = 0; ok && t < num_tasks; ++it) {
-        const Task k = decode_task(args, n_tiles, t);
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        Task k;
+        if (!next_task(it, k)) break;
+        ptx::mbar_arrive(taken_bar(it % kQ));
         const int wrow = k.e * args.N + k.nt * kLBN;
-        int t_next = num_tasks;
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (kb == claim_at) {
-            t_next = atomicAdd(args.counter, 1);
-            if (!publish(it + 1, t_next)) { ok = false; break; }
-          }
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { ok = false; break; }
           if constexpr (I8) {
             const uint32_t dst = sbase + stage * kTile8;  // weight codes
@@ -317,7 +332,6 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
           ++issued;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
-        t = t_next;
       }
 #pragma unroll
       for (int s = 0; s < kStages; ++s) {
@@ -333,9 +347,8 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       uint32_t aphase = 0;
       bool ok = true;
       for (int it = 0; ok; ++it) {
-        const int t = next_task(it);
-        if (t < 0 || t >= num_tasks) break;
-        const Task k = decode_task(args, n_tiles, t);
+        Task k;
+        if (!next_task(it, k)) break;
         const int slabs = (k.rows + kI8Slab - 1) / kI8Slab;  // only the 32-row slabs holding the task's rows
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait(aempty_bar(astage), aphase ^ 1u, abort_flag)) { ok = false; break; }
@@ -374,8 +387,8 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       uint32_t phase = 0, ophase = 0;
       bool ok = true;
       for (int it = 0; ok; ++it) {
-        const int t = next_task(it);
-        if (t < 0 || t >= num_tasks) break;
+        Task k;
+        if (!next_task(it, k)) break;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
           const uint8_t* src = smem + stage * kTile8 + r * 128;
@@ -412,11 +425,11 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       uint32_t phase = 0, ophase = 0, aphase = 0;
       bool ok = true;
       for (int it = 0; ok; ++it) {
-        const int t = next_task(it);
-        if (t < 0 || t >= num_tasks) break;
+        Task k;
+        if (!next_task(it, k)) break;
         uint32_t idesc_t = idesc;
         if constexpr (I8) {  // transposed product: N = the task's tokens, rounded up to 16
-          const int n_tok = (decode_task(args, n_tiles, t).rows + 15) & ~15;
+          const int n_tok = (k.rows + 15) & ~15;
           idesc_t = (idesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(n_tok >> 3) << 17);
         }
         const int b = it & 1;
@@ -476,9 +489,8 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       // Lane r holds output channel nt * 128 + r; column m holds the task's token m. A warp's
       // store for one token writes 32 consecutive channels of its output row.
       for (int it = 0;; ++it) {
-        const int t = next_task(it);
-        if (t < 0 || t >= num_tasks) break;
-        const Task k = decode_task(args, n_tiles, t);
+        Task k;
+        if (!next_task(it, k)) break;
         const int b = it & 1;
         float* sc = scl + b * kLBN;
         if (!second) sc[r] = r < k.rows ? __ldg(args.sx + k.row0 + r) : 0.f;
@@ -516,9 +528,8 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       }
     } else {
     for (int it = 0;; ++it) {
-      const int t = next_task(it);
-      if (t < 0 || t >= num_tasks) break;
-      const Task k = decode_task(args, n_tiles, t);
+      Task k;
+      if (!next_task(it, k)) break;
       const int b = it & 1;
       float* sc = scl + b * kLBN;
       if (!second) sc[r] = __ldg(args.sw + static_cast<size_t>(k.e) * args.N + k.nt * kLBN + r);
@@ -570,13 +581,26 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 5) ptx::tmem_dealloc(tmem_base, lowp_tmem_cols<I8>());
-  if (tid == 0 && *abort_flag) report_error(args.err, MOE_DEVERR_TIMEOUT);
+  if (tid == 0) {
+    if (*abort_flag) report_error(args.err, MOE_DEVERR_TIMEOUT);
+    // Every claim of this CTA has returned (the barrier above); the last CTA out
+    // leaves both counters zero for the next call on this workspace.
+    __threadfence();
+    if (atomicAdd(args.exit_ticket, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(args.counter, 0);
+      atomicExch(args.exit_ticket, 0);
+    }
+  }
 }
 
 }  // namespace
 
-// Header, per-expert row-block prefix, then (INT8 inputs) the fp16 copy of the activation codes.
-size_t lowp_meta_bytes(int E) { return kWsHeader + align_up(static_cast<size_t>(E + 1) * 4, 256); }
+// Header (error word, task counter, exit ticket), then (INT8 inputs) the fp16 copy of the
+// activation codes.
+size_t lowp_meta_bytes(int E) {
+  (void)E;
+  return kWsHeader;
+}
 size_t lowp_workspace_bytes(int M, int K, int E) {
   return lowp_meta_bytes(E) + align_up(static_cast<size_t>(M) * K * 2, 256);
 }
@@ -610,13 +634,8 @@ extern "C" moe_status_t gmm_lowp(const void* input, const void* weights, const f
   uint8_t* w = static_cast<uint8_t*>(ws);
   int* err = reinterpret_cast<int*>(w);
   int* counter = reinterpret_cast<int*>(w + 4);
-  int* num_tasks = reinterpret_cast<int*>(w + 8);
-  int32_t* mt_prefix = reinterpret_cast<int32_t*>(w + kWsHeader);
-  const int n_tiles = N / kLBN;
-  lowp_prep_kernel<<<1, 1024, 0, s>>>(expert_offsets, expert_sizes, E, M, n_tiles, mt_prefix, counter, num_tasks,
-                                      err);
-  moe_status_t st = launch_status();
-  if (st != MOE_OK) return st;
+  int* exit_ticket = reinterpret_cast<int*>(w + 8);
+  moe_status_t st = MOE_OK;
   CUtensorMap map_x, map_w;
   if (i8) {
     // widen the activation codes once; the kernel loads them as fp16 tiles (a
@@ -632,15 +651,27 @@ extern "C" moe_status_t gmm_lowp(const void* input, const void* weights, const f
   }
   if (!make_tmap_u8_2d(&map_w, weights, static_cast<uint64_t>(E) * N, K, true)) return MOE_ERR_CUDA;
   LowpArgs a{};
-  a.sx = scales_x; a.sw = scales_w; a.offsets = expert_offsets; a.sizes = expert_sizes; a.mt_prefix = mt_prefix;
-  a.counter = counter; a.num_tasks = num_tasks; a.out = out; a.err = err;
+  a.sx = scales_x; a.sw = scales_w; a.offsets = expert_offsets; a.sizes = expert_sizes;
+  a.counter = counter; a.exit_ticket = exit_ticket; a.out = out; a.err = err;
   a.M = M; a.K = K; a.N = N; a.E = E; a.out_f32 = out_dt == MOE_DT_F32;
   const void* fn = i8 ? reinterpret_cast<const void*>(gmm_lowp_kernel<true>)
                       : reinterpret_cast<const void*>(gmm_lowp_kernel<false>);
   if (!ensure_smem_attr(fn, static_cast<int>(kLSmem))) return MOE_ERR_CUDA;
-  if (i8)
-    gmm_lowp_kernel<true><<<num_sms(), lowp_threads<true>(), kLSmem, s>>>(map_x, map_w, a);
-  else
-    gmm_lowp_kernel<false><<<num_sms(), lowp_threads<false>(), kLSmem, s>>>(map_x, map_w, a);
+  // Programmatic dependent launch: the GEMM's CTAs set up (barriers, TMEM) while the
+  // kernel before them in the stream finishes, and wait in-kernel for its completion
+  // before touching global memory.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms());
+  cfg.blockDim = dim3(i8 ? lowp_threads<true>() : lowp_threads<false>());
+  cfg.dynamicSmemBytes = kLSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = i8 ? cudaLaunchKernelEx(&cfg, gmm_lowp_kernel<true>, map_x, map_w, a)
+                           : cudaLaunchKernelEx(&cfg, gmm_lowp_kernel<false>, map_x, map_w, a);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
   return launch_status();
 }

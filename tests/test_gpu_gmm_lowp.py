@@ -88,6 +88,32 @@ def test_gmm_int8_exact_integers():
         assert np.array_equal(got[off[e]:off[e + 1]], ref.astype(np.float64))
 
 
+@pytest.mark.parametrize("dt", ["i8", "e4m3"])
+def test_gmm_workspace_reused_across_calls(dt):
+    """The task counters live in the workspace: consecutive calls on one workspace (different
+    group layouts and sizes) each compute every row, and leave the counters zero."""
+    import mixture_experts_routing_grouped_gb300 as moe
+    rng = np.random.default_rng(11)
+    K, N, E = 256, 384, 5
+    ws = torch.zeros(moe.gmm_lowp_workspace_size(700, K, N, E), dtype=torch.uint8, device="cuda")
+    for sizes in ([100, 0, 300, 1, 299], [700, 0, 0, 0, 0], [1, 2, 3, 4, 5], [0, 0, 0, 0, 129]):
+        M = sum(sizes)
+        qx = _random_codes(rng, (M, K), dt)
+        qw = _random_codes(rng, (E, N, K), dt)
+        sx = rng.uniform(0.01, 0.1, M)
+        sw = rng.uniform(0.001, 0.01, (E, N))
+        off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+        out = moe.gmm_lowp(_to_dev(qx, dt), _to_dev(qw, dt), torch.from_numpy(sx.astype(np.float32)).cuda(),
+                           torch.from_numpy(sw.astype(np.float32)).cuda(), torch.from_numpy(off).cuda(),
+                           torch.from_numpy(np.asarray(sizes, dtype=np.int32)).cuda(), out_dtype=torch.float32,
+                           ws=ws)
+        torch.cuda.synchronize()
+        assert moe.moe_check_device_error(ws) == 0
+        assert torch.count_nonzero(ws[4:12]).item() == 0
+        ref = ogmm.gmm(qx, qw, sx.astype(np.float32), sw.astype(np.float32), off, sizes, dt)
+        _assert_close(out.cpu().numpy().astype(np.float64), ref, torch.float32)
+
+
 def test_gmm_inconsistent_metadata_is_reported_and_skipped():
     import mixture_experts_routing_grouped_gb300 as moe
     rng = np.random.default_rng(4)
