@@ -401,7 +401,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const size_t per = (args.clear_n4 + gridDim.x - 1) / gridDim.x;
       const size_t lo = per * blockIdx.x;
       const size_t hi = lo + per < args.clear_n4 ? lo + per : args.clear_n4;
-      for (size_t i = lo + tid; i < hi; i += 32 * kEpiWarps) args.clear[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      // evict-last: the zeroed rows stay in L2 through this kernel's weight stream
+      // until the down kernel reduces into them
+      const uint64_t pol = ptx::l2_policy_evict_last();
+      for (size_t i = lo + tid; i < hi; i += 32 * kEpiWarps)
+        ptx::st_f32x4(reinterpret_cast<float*>(args.clear + i), make_float4(0.f, 0.f, 0.f, 0.f), pol);
     }
     for (int it = 0;; ++it) {
       int t;

@@ -11,7 +11,8 @@
 // sorted order), so both operands arrive by TMA.
 //
 // Kernel shape (one persistent CTA per SM, 320 threads):
-//   warps 0-(P-1)  epilogue: TMEM -> registers -> shared staging -> fp32 atomics
+//   warps 0-(P-1)  epilogue: TMEM -> registers -> shared staging -> fp32 reductions
+//              (red.global.add, L2 evict-last)
 //              (TMEM lane quarter = warp % 4). The bf16 instance has P = 4 warps;
 //              the FP8 instance P = 8 (column half = warp / 4: two warps drain
 //              each accumulator row), so that the combine of a tile stays shorter
@@ -207,6 +208,9 @@ __global__ void __launch_bounds__(gemm_threads<F8>(), 1)
     const int chalf = warp >> 2;     // accumulator columns [kBN / kParts * chalf, ...) of this warp
     const int r = quarter * 32 + lane;  // accumulator row = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    // The accumulator rows are reduced into at L2 while the weights stream past:
+    // evict-last keeps them resident.
+    const uint64_t acc_pol = ptx::l2_policy_evict_last();
     int it = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
       const int b = it & 1;
@@ -280,8 +284,8 @@ __global__ void __launch_bounds__(gemm_threads<F8>(), 1)
             const int q = lane & 7;
             const float4 v = stg[rl * 8 + (q ^ (rl & 7))];
             if (trow[i] >= 0)
-              atomicAdd(reinterpret_cast<float4*>(args.y_acc + static_cast<size_t>(trow[i]) * args.H + nt * kBN +
-                                                  c * 32) + q, v);
+              ptx::red_add_f32x4(args.y_acc + static_cast<size_t>(trow[i]) * args.H + nt * kBN + c * 32 + 4 * q, v,
+                                 acc_pol);
           }
           __syncwarp();
         }
@@ -316,8 +320,8 @@ __global__ void __launch_bounds__(gemm_threads<F8>(), 1)
             const int trow = __shfl_sync(0xffffffffu, tok, rl);
             const float4 v = stg[rl * 8 + (q ^ (rl & 7))];
             if (trow >= 0)
-              atomicAdd(reinterpret_cast<float4*>(args.y_acc + static_cast<size_t>(trow) * args.H + nt * kBN +
-                                                  c * 32) + q, v);
+              ptx::red_add_f32x4(args.y_acc + static_cast<size_t>(trow) * args.H + nt * kBN + c * 32 + 4 * q, v,
+                                 acc_pol);
           }
           __syncwarp();
         }

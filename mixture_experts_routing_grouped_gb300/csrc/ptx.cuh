@@ -100,6 +100,27 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- L2 cache hints
+// Policy that marks lines evict-last in L2, for data read again soon after a large
+// stream passes through the cache (the combine's fp32 accumulator).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// dst[0..3] += v (four fp32 reductions, relaxed, GPU scope) under an L2 cache policy.
+__device__ __forceinline__ void red_add_f32x4(float* dst, float4 v, uint64_t pol) {
+  asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w), "l"(pol)
+               : "memory");
+}
+// dst[0..3] = v under an L2 cache policy.
+__device__ __forceinline__ void st_f32x4(float* dst, float4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w), "l"(pol)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async (gather)
 // 16-byte global->shared copy; src_bytes = 0 writes 16 zero bytes.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
