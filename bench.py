@@ -34,6 +34,7 @@ sys.path.insert(0, str(ROOT))
 METRIC = "MoE layer tokens/s + % BF16 tensor peak; decode weight-stream GB/s vs HBM"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+E2E_STREAMS = 4  # streams (each with its own buffers) that the end-to-end steps rotate over
 
 
 def load_peaks():
@@ -301,13 +302,16 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
     d2h = yh.numel() * 2 + twh.numel() * 4 + idh.numel() * 4
 
     # ---- the same, as a stream of steps: every step still copies its inputs from pinned host
-    # memory and its outputs back, but steps alternate between two CUDA streams with their own
-    # device buffers and workspaces, so that one step's copies (copy engines) overlap the other
-    # step's kernels (SMs). The window spans all K steps (no L2 flush: a step's working set, the
-    # 1.2 GB of weights, is far larger than L2); the figure is the serving throughput.
-    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+    # memory and its outputs back, but steps rotate over E2E_STREAMS CUDA streams with their
+    # own device buffers and workspaces, so that a step's copies (copy engines) overlap the
+    # other steps' kernels (SMs). With two streams a stream's output copy and next input copy
+    # (~90 + ~85 us) had to fit in one other step's kernels and held the steps back (396 us per
+    # step against 325 us without copies); with four they fit (331 us). The window spans all K
+    # steps (no L2 flush: a step's working set, the 1.2 GB of weights, is far larger than L2);
+    # the figure is the serving throughput.
+    streams = [torch.cuda.Stream(dev) for _ in range(E2E_STREAMS)]
     bufs = []
-    for _ in range(2):
+    for _ in range(E2E_STREAMS):
         bufs.append({"x": torch.empty_like(acts["x"]), "g": torch.empty_like(acts["gating"]),
                      "y": torch.empty_like(y), "tw": torch.empty_like(tw), "ids": torch.empty_like(ids),
                      "ws": torch.zeros_like(ws),
@@ -316,8 +320,8 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
                      "idh": torch.empty((cfg.T, cfg.topk), dtype=torch.int32).pin_memory()})
 
     def pipelined_step(i):
-        bf = bufs[i % 2]
-        with torch.cuda.stream(streams[i % 2]):
+        bf = bufs[i % E2E_STREAMS]
+        with torch.cuda.stream(streams[i % E2E_STREAMS]):
             bf["x"].copy_(xh, non_blocking=True)
             bf["g"].copy_(gh, non_blocking=True)
             moe.moe_fused_forward(bf["x"], bf["g"], W["w1"], W["w2"], cfg.topk, cfg.renormalize,
@@ -327,7 +331,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
             bf["twh"].copy_(bf["tw"], non_blocking=True)
             bf["idh"].copy_(bf["ids"], non_blocking=True)
 
-    for i in range(2 * args.warmup):
+    for i in range(E2E_STREAMS * args.warmup):
         pipelined_step(i)
     torch.cuda.synchronize()
     windows = []
@@ -346,7 +350,7 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
         b.synchronize()
         windows.append(a.elapsed_time(b) / K)
     e2e_ms = max_over_ranks(torch, statistics.median(windows), dev)
-    for i in range(2):  # every stream's last step returned the layer's outputs
+    for i in range(E2E_STREAMS):  # every stream's last step returned the layer's outputs
         assert torch.equal(bufs[i]["idh"], ids.cpu()), "pipelined steps returned other routing ids"
 
     # ---- roofline of the dominant kernel (gate_up grouped GEMM)
@@ -384,9 +388,9 @@ def run_ours(args, peaks, peaks_kind, rank, world, local_rank):
         "e2e": {"value": round(job_tokens_per_s(cfg.T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "method": f"{K} steps through moe_fused_forward, each copying x and logits from pinned host "
-                          "memory and y, weights and ids back, alternating between two streams with their own "
-                          "device buffers (one step's copies overlap the other's kernels); one window over all "
-                          "steps, median of 3"},
+                          "memory and y, weights and ids back, rotating over "
+                          f"{E2E_STREAMS} streams with their own device buffers (a step's copies overlap the "
+                          "other steps' kernels); one window over all steps, median of 3"},
         "e2e_serial": {"value": round(job_tokens_per_s(cfg.T, world, e2e_serial_ms), 1), "unit": "tokens/s",
                        "ms_per_step": round(e2e_serial_ms, 4),
                        "method": "one step at a time on one stream: copies in, layer, copies out, L2 flushed "
