@@ -53,6 +53,8 @@ __global__ void __launch_bounds__(kAlignThreads)
                             int32_t* __restrict__ sorted_ids, int32_t* __restrict__ sorted_tok,
                             int32_t* __restrict__ expert_ids, int32_t* __restrict__ expert_offsets,
                             int32_t* __restrict__ ntpp, int* __restrict__ err, int* __restrict__ zero_word) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int hist[MOE_MAX_EXPERTS];
   __shared__ int warp_tot[kAlignWarps];
   __shared__ int is_last;
@@ -167,6 +169,8 @@ __global__ void __launch_bounds__(kAlignThreads)
     align_scatter_kernel(const int32_t* __restrict__ ids, int num_pairs, int E, int chunk,
                          const int32_t* __restrict__ chunk_base, int* __restrict__ done,
                          int32_t* __restrict__ sorted_ids, int32_t* __restrict__ sorted_tok, int topk) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int cur[];  // [kAlignWarps][E]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
@@ -220,6 +224,8 @@ constexpr int kSmallScan = 65536;
 __global__ void __launch_bounds__(kAlignThreads)
     align_hist_kernel(const int32_t* __restrict__ ids, int num_pairs, int E, int chunk,
                       int32_t* __restrict__ hists, int* __restrict__ err, int* __restrict__ zero_word) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int hist[MOE_MAX_EXPERTS];
   const int tid = threadIdx.x;
   if (zero_word && blockIdx.x == 0 && tid == 0) *zero_word = 0;
@@ -244,6 +250,8 @@ __global__ void __launch_bounds__(kAlignThreads)
                               int32_t* __restrict__ sorted_ids, int32_t* __restrict__ sorted_tok, int topk,
                               int32_t* __restrict__ expert_ids, int32_t* __restrict__ expert_offsets,
                               int32_t* __restrict__ ntpp, int* __restrict__ zero_word) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int sm[];
   int* cur = sm;                              // [kAlignWarps][E] write cursors
   int* tot = cur + kAlignWarps * E;           // [E] pairs per expert
@@ -384,30 +392,28 @@ moe_status_t launch_align(const int32_t* ids, int num_pairs, int E, int block_m,
   int* done = static_cast<int*>(scratch);
   int32_t* chunk_base = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + 256);
   if (p.nchunks * E <= kSmallScan) {
-    align_hist_kernel<<<p.nchunks, kAlignThreads, 0, s>>>(ids, num_pairs, E, p.chunk, chunk_base, err, zero_word);
-    moe_status_t st = launch_status();
+    moe_status_t st = launch_pdl(align_hist_kernel, dim3(p.nchunks), dim3(kAlignThreads), 0, s, ids, num_pairs, E,
+                                 p.chunk, chunk_base, err, zero_word);
     if (st != MOE_OK) return st;
     const size_t smem = static_cast<size_t>(kAlignWarps + 3) * E * sizeof(int);
     if (!ensure_smem_attr(reinterpret_cast<const void*>(align_scan_scatter_kernel),
                           static_cast<int>(static_cast<size_t>(kAlignWarps + 3) * MOE_MAX_EXPERTS * sizeof(int))))
       return MOE_ERR_CUDA;
-    align_scan_scatter_kernel<<<p.nchunks, kAlignThreads, smem, s>>>(
-        ids, num_pairs, E, block_m, cap, p.chunk, p.nchunks, chunk_base, p.nchunks, 1, sorted_ids, sorted_tok,
-        topk > 0 ? topk : 1, expert_ids, expert_offsets, ntpp, nullptr);
-    return launch_status();
+    return launch_pdl(align_scan_scatter_kernel, dim3(p.nchunks), dim3(kAlignThreads), smem, s, ids, num_pairs, E,
+                      block_m, cap, p.chunk, p.nchunks, static_cast<const int32_t*>(chunk_base), p.nchunks, 1,
+                      sorted_ids, sorted_tok, topk > 0 ? topk : 1, expert_ids, expert_offsets, ntpp,
+                      static_cast<int*>(nullptr));
   }
-  align_count_scan_kernel<<<p.nchunks, kAlignThreads, 0, s>>>(ids, num_pairs, E, block_m, cap, p.chunk, p.nchunks,
-                                                              chunk_base, done, sorted_ids, sorted_tok,
-                                                              expert_ids, expert_offsets, ntpp, err, zero_word);
-  moe_status_t st = launch_status();
+  moe_status_t st = launch_pdl(align_count_scan_kernel, dim3(p.nchunks), dim3(kAlignThreads), 0, s, ids, num_pairs,
+                               E, block_m, cap, p.chunk, p.nchunks, chunk_base, done, sorted_ids, sorted_tok,
+                               expert_ids, expert_offsets, ntpp, err, zero_word);
   if (st != MOE_OK) return st;
   const size_t smem = static_cast<size_t>(kAlignWarps) * E * sizeof(int);
   if (!ensure_smem_attr(reinterpret_cast<const void*>(align_scatter_kernel),
                         static_cast<int>(static_cast<size_t>(kAlignWarps) * MOE_MAX_EXPERTS * sizeof(int))))
     return MOE_ERR_CUDA;
-  align_scatter_kernel<<<p.nchunks, kAlignThreads, smem, s>>>(ids, num_pairs, E, p.chunk, chunk_base, done,
-                                                              sorted_ids, sorted_tok, topk > 0 ? topk : 1);
-  return launch_status();
+  return launch_pdl(align_scatter_kernel, dim3(p.nchunks), dim3(kAlignThreads), smem, s, ids, num_pairs, E, p.chunk,
+                    static_cast<const int32_t*>(chunk_base), done, sorted_ids, sorted_tok, topk > 0 ? topk : 1);
 }
 
 // Scratch for align run on the routing kernel's counts of T tokens: 256 bytes, then at most
@@ -440,10 +446,9 @@ moe_status_t launch_align_from_tile_hists(const int32_t* ids, int num_pairs, int
   if (!ensure_smem_attr(reinterpret_cast<const void*>(align_scan_scatter_kernel),
                         static_cast<int>(static_cast<size_t>(kAlignWarps + 3) * MOE_MAX_EXPERTS * sizeof(int))))
     return MOE_ERR_CUDA;
-  align_scan_scatter_kernel<<<p.nchunks, kAlignThreads, smem, s>>>(
-      ids, num_pairs, E, block_m, cap, p.chunk, p.nchunks, tile_hist, tile_rows, p.chunk / pairs_per_tile,
-      sorted_ids, sorted_tok, topk > 0 ? topk : 1, expert_ids, expert_offsets, ntpp, zero_word);
-  return launch_status();
+  return launch_pdl(align_scan_scatter_kernel, dim3(p.nchunks), dim3(kAlignThreads), smem, s, ids, num_pairs, E,
+                    block_m, cap, p.chunk, p.nchunks, tile_hist, tile_rows, p.chunk / pairs_per_tile, sorted_ids,
+                    sorted_tok, topk > 0 ? topk : 1, expert_ids, expert_offsets, ntpp, zero_word);
 }
 
 }  // namespace moe

@@ -94,6 +94,8 @@ Plan choose_plan(int T, int E, int topk) {
 // time left the kernel latency-bound on the just-written, L2-resident rows).
 __global__ void __launch_bounds__(256) cast_f32_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
                                                             size_t n4) {
+  pdl_trigger();
+  pdl_wait();
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4; i += 4 * stride) {
     float4 v[4];
@@ -307,9 +309,9 @@ extern "C" moe_status_t moe_fused_forward(const void* x, const float* gating, co
                           y_acc, err, num_pairs, topk, L.cap, H, I, E, s);
   if (st != MOE_OK) return st;
   stage_mark(4, s);
-  cast_f32_bf16_kernel<<<grid_for(n4), 256, 0, s>>>(reinterpret_cast<const float4*>(y_acc),
-                                                    reinterpret_cast<uint2*>(y), n4);
-  if ((st = launch_status()) != MOE_OK) return st;
+  st = launch_pdl(cast_f32_bf16_kernel, dim3(grid_for(n4)), dim3(256), 0, s,
+                  reinterpret_cast<const float4*>(y_acc), reinterpret_cast<uint2*>(y), n4);
+  if (st != MOE_OK) return st;
   stage_mark(5, s);
   return MOE_OK;
 }
@@ -405,9 +407,9 @@ extern "C" moe_status_t moe_fused_forward_fp8(const void* x, const float* gating
   if (st != MOE_OK) return st;
   stage_mark(6, s);
   const size_t n4 = static_cast<size_t>(T) * H / 4;
-  cast_f32_bf16_kernel<<<grid_for(n4), 256, 0, s>>>(reinterpret_cast<const float4*>(y_acc),
-                                                    reinterpret_cast<uint2*>(y), n4);
-  if ((st = launch_status()) != MOE_OK) return st;
+  st = launch_pdl(cast_f32_bf16_kernel, dim3(grid_for(n4)), dim3(256), 0, s,
+                  reinterpret_cast<const float4*>(y_acc), reinterpret_cast<uint2*>(y), n4);
+  if (st != MOE_OK) return st;
   stage_mark(7, s);
   return MOE_OK;
 }

@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
+  pdl_trigger();
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(full_bar(s), 2);  // weight expect_tx arrive + the slot's gather warp
@@ -178,7 +179,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
     ptx::tmem_relinquish();
-  } else if (warp == 1) {
+  } else if (warp == kTmaWarp) {
+    ptx::prefetch_tmap(&map_b);
+  }
+  pdl_wait();  // from here on: reads of what the kernels before this one wrote
+  if (warp == 1) {
     const int per = (args.E + 31) / 32;
     const int e0 = lane * per;
     int sum = 0;
@@ -205,8 +210,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     if (lane == 31) pfx[args.E] = incl;
-  } else if (warp == kTmaWarp) {
-    ptx::prefetch_tmap(&map_b);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -500,8 +503,7 @@ moe_status_t launch_gate_up(const CUtensorMap& map_b, const pair::GemmArgs& a, c
   using namespace pair;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_gate_up_kernel<F8>), static_cast<int>(kGemmSmem)))
     return MOE_ERR_CUDA;
-  moe_gate_up_kernel<F8><<<num_sms(), kGemmThreads, kGemmSmem, s>>>(map_b, a);
-  return launch_status();
+  return launch_pdl(moe_gate_up_kernel<F8>, dim3(num_sms()), dim3(kGemmThreads), kGemmSmem, s, map_b, a);
 }
 
 }  // namespace

@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(gemm_threads<F8>(), 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
+  pdl_trigger();
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(gemm_threads<F8>(), 1)
     ptx::prefetch_tmap(&map_b);
     ptx::prefetch_tmap(&map_a);
   }
+  pdl_wait();  // from here on: reads of what the kernels before this one wrote
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -435,8 +437,7 @@ template <bool F8>
 moe_status_t launch_down(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& a, cudaStream_t s) {
   if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_down_kernel<F8>), static_cast<int>(kGemmSmem)))
     return MOE_ERR_CUDA;
-  moe_down_kernel<F8><<<num_sms(), gemm_threads<F8>(), kGemmSmem, s>>>(map_a, map_b, a);
-  return launch_status();
+  return launch_pdl(moe_down_kernel<F8>, dim3(num_sms()), dim3(gemm_threads<F8>()), kGemmSmem, s, map_a, map_b, a);
 }
 
 }  // namespace

@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  pdl_trigger();
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(full_bar(s), MODE == kSwGateUp ? 32 + 1 : 1);
@@ -159,7 +160,12 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
   if (warp == C::kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(const_cast<uint32_t*>(tmem_slot)), 512);
     ptx::tmem_relinquish();
-  } else if (warp == 1) {
+  } else if (warp == 4) {
+    ptx::prefetch_tmap(&map_w);
+    if (MODE == kSwDown) ptx::prefetch_tmap(&map_b);
+  }
+  pdl_wait();  // from here on: reads of what the kernels before this one wrote
+  if (warp == 1) {
     // task prefix over experts: pfx[e] = sum_{e' < e} n_wb * ntb(e')
     const int per_lane = (args.E + 31) / 32;
     const int e0 = lane * per_lane;
@@ -189,9 +195,6 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
       }
     }
     if (lane == 31) pfx[args.E] = incl;
-  } else if (warp == 4) {
-    ptx::prefetch_tmap(&map_w);
-    if (MODE == kSwDown) ptx::prefetch_tmap(&map_b);
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -418,8 +421,7 @@ moe_status_t launch_swap_impl(const CUtensorMap& mw, const CUtensorMap& mb, cons
   using C = SwapCfg<NMAX>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_swap_kernel<MODE, NMAX, F8>), static_cast<int>(C::kSmem)))
     return MOE_ERR_CUDA;
-  moe_swap_kernel<MODE, NMAX, F8><<<num_sms(), C::kThreads, C::kSmem, s>>>(mw, mb, a);
-  return launch_status();
+  return launch_pdl(moe_swap_kernel<MODE, NMAX, F8>, dim3(num_sms()), dim3(C::kThreads), C::kSmem, s, mw, mb, a);
 }
 
 }  // namespace

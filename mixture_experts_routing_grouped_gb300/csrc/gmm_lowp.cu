@@ -119,6 +119,8 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
 // INT8 activation codes -> fp16 (exact), 16 codes per thread and step.
 __global__ void __launch_bounds__(256) widen_i8_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                                        size_t n16) {
+  pdl_trigger();
+  pdl_wait();
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const uint4 v = __ldg(src + i);
@@ -167,6 +169,7 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
   volatile int* tq = reinterpret_cast<volatile int*>(ctl + 512 + 2 * kLBN * 4);  // [kQ][4] claimed tasks
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
   const int n_tiles = args.N / kLBN;
   const int kblocks = args.K / kLBK;
   constexpr int kConvThreads = I8 ? 32 * kI8ConvWarps : 0;
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
   // Launched as a programmatic dependent of the kernel before it in the stream (for
   // INT8 the activation widening): the prologue above overlapped that kernel; nothing
   // in global memory is read or written before it has completed.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();
 
   // Task queue consumer: the claiming thread decodes every task once and publishes
   // it whole, so that no consumer waits on the dependent global loads of a decode.
@@ -643,8 +646,9 @@ extern "C" moe_status_t gmm_lowp(const void* input, const void* weights, const f
     void* xh = w + lowp_meta_bytes(E);
     const size_t n16 = static_cast<size_t>(M) * K / 16;
     const int grid = static_cast<int>(std::min<size_t>((n16 + 255) / 256, static_cast<size_t>(num_sms()) * 8));
-    widen_i8_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(input), static_cast<uint4*>(xh), n16);
-    if ((st = launch_status()) != MOE_OK) return st;
+    st = launch_pdl(widen_i8_kernel, dim3(grid), dim3(256), 0, s, static_cast<const uint4*>(input),
+                    static_cast<uint4*>(xh), n16);
+    if (st != MOE_OK) return st;
     if (!make_tmap_bf16_2d_rows(&map_x, xh, M, K, kI8Slab)) return MOE_ERR_CUDA;
   } else if (!make_tmap_u8_2d(&map_x, input, M, K, true)) {
     return MOE_ERR_CUDA;
@@ -657,21 +661,7 @@ extern "C" moe_status_t gmm_lowp(const void* input, const void* weights, const f
   const void* fn = i8 ? reinterpret_cast<const void*>(gmm_lowp_kernel<true>)
                       : reinterpret_cast<const void*>(gmm_lowp_kernel<false>);
   if (!ensure_smem_attr(fn, static_cast<int>(kLSmem))) return MOE_ERR_CUDA;
-  // Programmatic dependent launch: the GEMM's CTAs set up (barriers, TMEM) while the
-  // kernel before them in the stream finishes, and wait in-kernel for its completion
-  // before touching global memory.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_sms());
-  cfg.blockDim = dim3(i8 ? lowp_threads<true>() : lowp_threads<false>());
-  cfg.dynamicSmemBytes = kLSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = i8 ? cudaLaunchKernelEx(&cfg, gmm_lowp_kernel<true>, map_x, map_w, a)
-                           : cudaLaunchKernelEx(&cfg, gmm_lowp_kernel<false>, map_x, map_w, a);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return launch_status();
+  if (i8)
+    return launch_pdl(gmm_lowp_kernel<true>, dim3(num_sms()), dim3(lowp_threads<true>()), kLSmem, s, map_x, map_w, a);
+  return launch_pdl(gmm_lowp_kernel<false>, dim3(num_sms()), dim3(lowp_threads<false>()), kLSmem, s, map_x, map_w, a);
 }

@@ -157,6 +157,8 @@ template <typename T, bool E4M3>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const T* __restrict__ x, int M, int K,
                                                          uint8_t* __restrict__ q, float* __restrict__ scales,
                                                          const int* __restrict__ rows_dev) {
+  pdl_trigger();
+  pdl_wait();
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= M || (rows_dev && row >= __ldg(rows_dev))) return;
@@ -223,6 +225,8 @@ template <typename T, bool E4M3, int L, int C>
 __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const T* __restrict__ x, int M, int K,
                                                              uint8_t* __restrict__ q, float* __restrict__ scales,
                                                              const int* __restrict__ rows_dev) {
+  pdl_trigger();
+  pdl_wait();
   static_assert(4 * C <= 32, "one flag bit per pair of a lane's chunks");
   const int gl = blockIdx.x * blockDim.x + threadIdx.x;
   const int row = gl / L;
@@ -278,7 +282,8 @@ __global__ void __launch_bounds__(256) quant_rows_reg_kernel(const T* __restrict
 template <typename T, bool E4M3, int L, int C>
 void launch_reg(const T* x, int M, int K, uint8_t* q, float* s, cudaStream_t st, const int* rows_dev) {
   const int rows_per_block = 256 / L;
-  quant_rows_reg_kernel<T, E4M3, L, C><<<cdiv(M, rows_per_block), 256, 0, st>>>(x, M, K, q, s, rows_dev);
+  (void)launch_pdl(quant_rows_reg_kernel<T, E4M3, L, C>, dim3(cdiv(M, rows_per_block)), dim3(256), 0, st, x, M, K, q,
+                   s, rows_dev);
 }
 
 // Lanes per row: the fewest (>= 8) that keep a lane's chunks within C (8 for bf16
@@ -291,7 +296,7 @@ void launch_quant_t(const T* x, int M, int K, uint8_t* q, float* s, cudaStream_t
   if (K <= 8 * 8 * C) launch_reg<T, E4M3, 8, C>(x, M, K, q, s, st, rows_dev);
   else if (K <= 8 * 16 * C) launch_reg<T, E4M3, 16, C>(x, M, K, q, s, st, rows_dev);
   else if (K <= 8 * 32 * C) launch_reg<T, E4M3, 32, C>(x, M, K, q, s, st, rows_dev);
-  else quant_rows_kernel<T, E4M3><<<cdiv(M, 8), 256, 0, st>>>(x, M, K, q, s, rows_dev);
+  else (void)launch_pdl(quant_rows_kernel<T, E4M3>, dim3(cdiv(M, 8)), dim3(256), 0, st, x, M, K, q, s, rows_dev);
 }
 
 template <typename T>

@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(256) grouped_topk_fast_kernel(const float* __r
                                                                 int topk_group, int topk, int scoring, int renorm,
                                                                 float rsf, float* __restrict__ out_w,
                                                                 int32_t* __restrict__ out_ids, RouteZero zero) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int E = 32 * VPL;
   const int token = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -203,6 +205,8 @@ __global__ void __launch_bounds__(256) grouped_topk_kernel(const float* __restri
                                                            int topk_group, int topk, int scoring, int renorm,
                                                            float rsf, float* __restrict__ out_w,
                                                            int32_t* __restrict__ out_ids, RouteZero zero) {
+  pdl_trigger();
+  pdl_wait();
   const int token = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (token >= T) return;
@@ -384,6 +388,8 @@ __global__ void __launch_bounds__(kSegThreads, 6) grouped_topk_seg_kernel(const 
                                                                           float* __restrict__ out_w,
                                                                           int32_t* __restrict__ out_ids,
                                                                           RouteZero zero) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int kRowBytes = P * 4;
   constexpr int kChunks = P / 4;  // 16-byte chunks per row, = chunks loaded per thread
   constexpr int V = P / F;        // phase-2 values per lane
@@ -677,6 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_topk_tpt_kernel(const __g
                                                                       float rsf, float* __restrict__ out_w,
                                                                       int32_t* __restrict__ out_ids, int* err,
                                                                       int32_t* __restrict__ tile_hist) {
+  pdl_trigger();
+  pdl_wait();
   using S = Shape<E>;
   constexpr int P = E / G;              // experts per group
   constexpr int UPG = P / 8;            // units per group
@@ -916,15 +924,14 @@ int seg_lanes(int E, int G, int k) {
 }
 
 template <int P, int L, int F>
-void launch_seg_f(const float* gating, int T, int G, int kg, int k, int scoring, int renorm, float rsf, float* w,
-                  int32_t* ids, const RouteZero& z, cudaStream_t s) {
+moe_status_t launch_seg_f(const float* gating, int T, int G, int kg, int k, int scoring, int renorm, float rsf,
+                          float* w, int32_t* ids, const RouteZero& z, cudaStream_t s) {
   const int grid = cdiv(T, kSegThreads / L);
   if (k == 8 && L >= 8)
-    grouped_topk_seg_kernel<P, L, F, 8><<<grid, kSegThreads, 0, s>>>(gating, T, G, kg, k, scoring, renorm, rsf, w,
-                                                                     ids, z);
-  else
-    grouped_topk_seg_kernel<P, L, F, 0><<<grid, kSegThreads, 0, s>>>(gating, T, G, kg, k, scoring, renorm, rsf, w,
-                                                                     ids, z);
+    return launch_pdl(grouped_topk_seg_kernel<P, L, F, 8>, dim3(grid), dim3(kSegThreads), 0, s, gating, T, G, kg, k,
+                      scoring, renorm, rsf, w, ids, z);
+  return launch_pdl(grouped_topk_seg_kernel<P, L, F, 0>, dim3(grid), dim3(kSegThreads), 0, s, gating, T, G, kg, k,
+                    scoring, renorm, rsf, w, ids, z);
 }
 
 template <int P, int L>
@@ -933,26 +940,27 @@ moe_status_t launch_seg(const float* gating, int T, int G, int kg, int k, int sc
   // F = G / topk_group lanes share a selected row in phase 2 (1 when that is not
   // 2 or 4, or leaves fewer than 4 values per lane)
   const int F = (G % kg == 0) ? G / kg : 1;
-  if (F == 2 && P >= 8) launch_seg_f<P, L, 2>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
-  else if (F == 4 && P >= 16) launch_seg_f<P, L, 4>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
-  else launch_seg_f<P, L, 1>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
-  return launch_status();
+  if (F == 2 && P >= 8) return launch_seg_f<P, L, 2>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  if (F == 4 && P >= 16) return launch_seg_f<P, L, 4>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  return launch_seg_f<P, L, 1>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
 }
 
 template <int VPL>
-void launch_fast(const float* gating, int T, int G, int kg, int k, int scoring, int renorm, float rsf, float* w,
-                 int32_t* ids, const RouteZero& z, cudaStream_t s) {
+moe_status_t launch_fast(const float* gating, int T, int G, int kg, int k, int scoring, int renorm, float rsf,
+                         float* w, int32_t* ids, const RouteZero& z, cudaStream_t s) {
   const int threads = 256;
   const int blocks = cdiv(T, threads / 32);
-  grouped_topk_fast_kernel<VPL><<<blocks, threads, 0, s>>>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z);
+  return launch_pdl(grouped_topk_fast_kernel<VPL>, dim3(blocks), dim3(threads), 0, s, gating, T, G, kg, k, scoring,
+                    renorm, rsf, w, ids, z);
 }
 
 template <int VPL>
-void launch_topk(const float* gating, int T, int E, int G, int kg, int k, int scoring, int renorm, float rsf,
-                 float* w, int32_t* ids, const RouteZero& z, cudaStream_t s) {
+moe_status_t launch_topk(const float* gating, int T, int E, int G, int kg, int k, int scoring, int renorm, float rsf,
+                         float* w, int32_t* ids, const RouteZero& z, cudaStream_t s) {
   const int threads = 256;
   const int blocks = cdiv(T, threads / 32);
-  grouped_topk_kernel<VPL><<<blocks, threads, 0, s>>>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z);
+  return launch_pdl(grouped_topk_kernel<VPL>, dim3(blocks), dim3(threads), 0, s, gating, T, E, G, kg, k, scoring,
+                    renorm, rsf, w, ids, z);
 }
 
 // Thread-per-token kernel instances: (E, G, topk_group) with topk = 8.
@@ -967,8 +975,8 @@ moe_status_t launch_tpt(const float* gating, int T, int scoring, int renorm, flo
   const int ntiles = cdiv(T, tpt::kTile);
   const int sms = num_sms() > 0 ? num_sms() : 148;
   const int grid = ntiles < sms ? ntiles : sms;
-  kernel<<<grid, tpt::kThreads, smem, s>>>(map, T, ntiles, scoring, renorm, rsf, w, ids, err, tile_hist);
-  return launch_status();
+  return launch_pdl(kernel, dim3(grid), dim3(tpt::kThreads), smem, s, map, T, ntiles, scoring, renorm, rsf, w, ids,
+                    err, tile_hist);
 }
 
 bool tpt_applies(int T, int E, int G, int kg, int k, const void* w, const void* ids) {
@@ -1082,23 +1090,22 @@ moe_status_t launch_grouped_topk(const float* gating, int T, int E, int G, int k
   const bool pow2_groups = (G & (G - 1)) == 0;
   if (pow2_groups) {
     switch (E) {
-      case 32: launch_fast<1>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s); return launch_status();
-      case 64: launch_fast<2>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s); return launch_status();
-      case 128: launch_fast<4>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s); return launch_status();
-      case 256: launch_fast<8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s); return launch_status();
-      case 512: launch_fast<16>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s); return launch_status();
-      case 1024: launch_fast<32>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s); return launch_status();
+      case 32: return launch_fast<1>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      case 64: return launch_fast<2>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      case 128: return launch_fast<4>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      case 256: return launch_fast<8>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      case 512: return launch_fast<16>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+      case 1024: return launch_fast<32>(gating, T, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
       default: break;
     }
   }
   const int per_lane = cdiv(E, 32);
-  if (per_lane <= 1) launch_topk<1>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
-  else if (per_lane <= 2) launch_topk<2>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
-  else if (per_lane <= 4) launch_topk<4>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
-  else if (per_lane <= 8) launch_topk<8>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
-  else if (per_lane <= 16) launch_topk<16>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
-  else launch_topk<32>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
-  return launch_status();
+  if (per_lane <= 1) return launch_topk<1>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  if (per_lane <= 2) return launch_topk<2>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  if (per_lane <= 4) return launch_topk<4>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  if (per_lane <= 8) return launch_topk<8>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  if (per_lane <= 16) return launch_topk<16>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
+  return launch_topk<32>(gating, T, E, G, kg, k, scoring, renorm, rsf, w, ids, z, s);
 }
 
 }  // namespace moe

@@ -50,6 +50,8 @@ int router_ksplit(int T, int H, int E) {
 __global__ void __launch_bounds__(kRThreads) router_logits_kernel(const __nv_bfloat16* __restrict__ x,
                                                                   const float* __restrict__ wg, int T, int H, int E,
                                                                   int ksplit, float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ __align__(16) float xs[2][kRT][kRPad];
   __shared__ __align__(16) float wsm[2][kRE][kRPad];
   const int tid = threadIdx.x;
@@ -142,6 +144,8 @@ __global__ void __launch_bounds__(kRThreads) router_logits_kernel(const __nv_bfl
 // logits[i] = part[0][i] + part[1][i] + ... + part[ksplit - 1][i], in that order.
 __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restrict__ part, size_t n, int ksplit,
                                                             float* __restrict__ logits) {
+  pdl_trigger();
+  pdl_wait();
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n; i += stride) {
     float s = part[i];
@@ -185,16 +189,17 @@ extern "C" moe_status_t moe_router_topk(const void* x, const float* w_gate, int 
   cudaStream_t s = as_stream(stream);
   float* part = ksplit > 1 ? static_cast<float*>(ws) : router_logits;
   const dim3 grid(cdiv(E, kRE), cdiv(T, kRT), ksplit);
-  router_logits_kernel<<<grid, kRThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(x), w_gate, T, H, E, ksplit,
-                                                  part);
-  if ((st = launch_status()) != MOE_OK) return st;
+  st = launch_pdl(router_logits_kernel, grid, dim3(kRThreads), 0, s, static_cast<const __nv_bfloat16*>(x), w_gate, T,
+                  H, E, ksplit, part);
+  if (st != MOE_OK) return st;
   if (ksplit > 1) {
     const size_t n = static_cast<size_t>(T) * E;
     const size_t want = (n + 255) / 256;
     const int sms = num_sms() > 0 ? num_sms() : 148;
     const int blocks = static_cast<int>(want < static_cast<size_t>(4 * sms) ? want : static_cast<size_t>(4 * sms));
-    router_reduce_kernel<<<blocks, 256, 0, s>>>(part, n, ksplit, router_logits);
-    if ((st = launch_status()) != MOE_OK) return st;
+    st = launch_pdl(router_reduce_kernel, dim3(blocks), dim3(256), 0, s, static_cast<const float*>(part), n, ksplit,
+                    router_logits);
+    if (st != MOE_OK) return st;
   }
   return launch_grouped_topk(router_logits, T, E, num_expert_group, topk_group, topk, scoring, renormalize,
                              routed_scaling_factor, topk_weights, topk_ids, s, nullptr, 0, nullptr, 0);
