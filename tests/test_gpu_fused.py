@@ -95,6 +95,11 @@ def _workload_check(cfg, rel_above_one=False):
     x = acts["x"].double().cpu().numpy()
     ry = omoe.expert_loop_forward(x, lambda e: _host_f64(W["w1"][e]), lambda e: _host_f64(W["w2"][e]), rw, rids)
     assert_moe_close(y.float().cpu().numpy(), ry, rel_above_one=rel_above_one)
+    # a second call on the same workspace: the kernels leave their scratch (counters,
+    # tickets) as they found it
+    y2, _, ids2 = _fused(cfg, acts, W, ws)
+    assert torch.equal(ids2, ids)
+    assert_moe_close(y2.float().cpu().numpy(), ry, rel_above_one=rel_above_one)
 
 
 def test_prefill_workload_whole():

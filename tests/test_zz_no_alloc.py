@@ -51,7 +51,10 @@ def test_noalloc_matches_workspace_entry_point(cfg):
         torch.cuda.synchronize()
         assert torch.equal(ids, ref_ids)
         assert_weights_close(w.cpu().numpy(), ref_w.cpu().numpy())
-        assert_moe_close(y.float().cpu().numpy(), ref_y.float().cpu().numpy())
+        # both are GPU results whose fp32 reductions may run in different orders (atomics),
+        # so a bf16 output can differ by one rounding step, which exceeds 2e-2 once |y| >= 4
+        # (the decode-like layer is scaled by 2.5)
+        assert_moe_close(y.float().cpu().numpy(), ref_y.float().cpu().numpy(), rel_above_one=True)
     # nothing went wrong on the device, and reading the scratch's error word clears it
     assert moe.moe_fused_forward_noalloc_check_error() == 0
 
