@@ -51,7 +51,7 @@ namespace {
 
 constexpr int kLBM = 128, kLBN = 128, kLBK = 128;      // K in elements (= bytes for 8-bit codes)
 constexpr int kTile8 = kLBM * kLBK;                     // 16 KB: one 8-bit operand tile
-constexpr int kF8Stages = 6;                            // fp8: 6 x (A 16 KB + B 16 KB)
+constexpr int kF8Stages = 7;                            // fp8: 7 x (A 16 KB + B 16 KB)
 constexpr int kTile16 = kLBM * kLBK * 2;                // 32 KB: one fp16 operand tile (2 column blocks)
 constexpr int kI8BStages = 6;                           // int8: 6 x 16 KB weight codes
 constexpr int kI8AStages = 4;                           // int8: 4 x 32 KB widened activations
@@ -65,7 +65,7 @@ constexpr int kI8OpCol = 2 * kLBN;                      // int8: first TMEM colu
 template <bool I8>
 constexpr int lowp_tmem_cols() { return I8 ? 512 : 2 * kLBN; }  // accumulators (+ int8 weight tiles)
 static_assert(kI8OpCol + kI8Ops * kLBK / 2 <= 512, "tensor memory columns");
-constexpr int kF8Ring = kF8Stages * 2 * kTile8;         // 192 KB
+constexpr int kF8Ring = kF8Stages * 2 * kTile8;         // 224 KB
 constexpr int kI8Ring = kI8AOff + kI8AStages * kTile16; // 224 KB
 constexpr size_t kLSmem = 1024 + kI8Ring + 512 + 2 * kLBN * 4 + kQ * 16;
 static_assert(kLSmem <= 232448, "shared memory per CTA");
