@@ -28,11 +28,11 @@
 // stays expert-major, so the CTAs in flight share an expert's weights and rows
 // in L2.
 //
-// A K step is 32 columns (64-byte rows, 64B swizzle), so that the 192 KB ring
-// has six 32 KB slots: a slot's gathered rows and weight tile land 1-3 us after
-// it is freed (L2 and HBM latency under load), and the six slots keep about
-// five K steps of MMA work queued against that, where three 64-column slots
-// left the MMA waiting for data for about 40 % of the kernel.
+// A K step is 32 columns (64-byte rows, 64B swizzle), so that the ring has
+// seven (bf16, up to 256 experts) or six 32 KB slots: a slot's gathered rows and
+// weight tile land 1-3 us after it is freed (L2 and HBM latency under load), and
+// the slots keep five to six K steps of MMA work queued against that, where
+// three 64-column slots left the MMA waiting for data for about 40 % of the kernel.
 //
 // The kernel is written in bytes of K: a K step is one 64-byte row segment of
 // both operands, 32 bf16 or 64 FP8-e4m3 values, and either way two MMAs of 32
@@ -42,12 +42,12 @@
 // the per-token-quantised activations and multiplies each accumulator by its
 // token's scale and its column's weight scale before the SwiGLU.
 //
-// Kernel shape (one persistent CTA per SM, 512 threads): warps 0-7 epilogue
-// (TMEM lane quarter = warp % 4, column chunks split between warps w and w+4, so
-// that the single accumulator is drained -- and the next tile's MMAs start --
-// in half the time), warp 8 sends the weight tile of every ring slot by TMA,
-// warps 9-14 gather (warp 9+s fills both row halves of ring slot s), warp 15
-// owns TMEM and issues the MMAs. A gather lane keeps the source offsets of its
+// Kernel shape (one persistent CTA per SM, 32 x (10 + slots) threads): warps 0-7
+// epilogue (TMEM lane quarter = warp % 4, column chunks split between warps w and
+// w+4, so that the single accumulator is drained -- and the next tile's MMAs
+// start -- in half the time), warp 8 sends the weight tile of every ring slot by
+// TMA, warps 9 .. 8+slots gather (warp 9+s fills both row halves of ring slot s),
+// the last warp owns TMEM and issues the MMAs. A gather lane keeps the source offsets of its
 // 32 rows of the tile in registers, so that its cp.async instructions issue
 // back to back (reading each offset from shared memory between them made the
 // gather issue-bound), and no gather lane waits for a TMA issue. The per-expert pair counts are prefix-summed in shared memory
@@ -67,23 +67,31 @@ namespace pair {
 constexpr int kHalf = 128;
 constexpr int kBN = 256;
 constexpr int kKBytes = 64;  // bytes of K per step: one 64-byte swizzle row (32 bf16 or 64 e4m3)
-constexpr int kStages = 6;
 constexpr int kHalfBytes = kHalf * kKBytes;
 constexpr int kABytes = 2 * kHalfBytes;
 constexpr int kBBytes = kBN * kKBytes;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each draining half of the column chunks
 constexpr int kTmaWarp = kEpiWarps;
 constexpr int kGatherWarp0 = kEpiWarps + 1;
-constexpr int kMmaWarp = kGatherWarp0 + kStages;  // one gather warp per ring slot
-constexpr int kGemmThreads = 32 * (kMmaWarp + 1);
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kQ = 4;                                        // claimed-tile queue entries
-constexpr int kQConsumers = kStages + 1 + kEpiWarps;          // gather warps, MMA thread, epilogue warps
-constexpr int kStagePitch = 18;  // 32-bit words per staged row: 16 bf16 pairs, 8-byte aligned rows
 constexpr int kScaleFloats = 128;  // FP8: per epilogue warp, gate and up channel scales of its two column chunks
-constexpr size_t kCtlBytes =
-    256 + 4 * (MOE_MAX_EXPERTS + 1) + 12 + kEpiWarps * 32 * kStagePitch * 4 + kEpiWarps * kScaleFloats * 4;
-constexpr size_t kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + kCtlBytes;
+constexpr int kDeepMaxExperts = 256;  // the seven-slot instance's expert table holds this many experts
+
+// One instance's ring depth and shared-memory layout. Seven slots (224 KB) leave room for
+// an expert table of kDeepMaxExperts experts; six slots hold the full MOE_MAX_EXPERTS table
+// and (FP8) the epilogue's channel scales.
+template <bool F8, int S>
+struct Shape {
+  static constexpr int kStages = S;
+  static constexpr int kMmaWarp = kGatherWarp0 + kStages;  // one gather warp per ring slot
+  static constexpr int kThreads = 32 * (kMmaWarp + 1);
+  static constexpr int kQConsumers = kStages + 1 + kEpiWarps;  // gather warps, MMA thread, epilogue warps
+  static constexpr int kPfxCap = ((S == 7 ? kDeepMaxExperts : MOE_MAX_EXPERTS) + 1 + 3) & ~3;
+  static constexpr size_t kCtlBytes = 320 + 4 * kPfxCap + (F8 ? kEpiWarps * kScaleFloats * 4 : 0);
+  static constexpr size_t kSmem = 1024 + kStages * (kABytes + kBBytes) + kCtlBytes;
+  static_assert(kSmem <= 232448, "gate_up shared memory exceeds the per-CTA maximum");
+};
 
 struct GemmArgs {
   const uint8_t* x;           // activations [T, K] (bf16, or e4m3 codes), K contiguous
@@ -130,9 +138,13 @@ __device__ __forceinline__ TileInfo decode_tile(const int* pfx, const int32_t* _
   return ti;
 }
 
-template <bool F8>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <bool F8, int S>
+__global__ void __launch_bounds__(Shape<F8, S>::kThreads, 1)
     moe_gate_up_kernel(const __grid_constant__ CUtensorMap map_b, const GemmArgs args) {
+  using Sh = Shape<F8, S>;
+  constexpr int kStages = Sh::kStages;
+  constexpr int kMmaWarp = Sh::kMmaWarp;
+  constexpr int kQConsumers = Sh::kQConsumers;
   constexpr int kElemsPerStep = F8 ? kKBytes : kKBytes / 2;  // K elements per step
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -149,12 +161,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t done_bar = bar_base + 8u * (2 * kStages + 2);
   auto qfull_bar = [&](int q) { return bar_base + 8u * (2 * kStages + 3 + q); };
   auto qempty_bar = [&](int q) { return bar_base + 8u * (2 * kStages + 3 + kQ + q); };
-  static_assert(8 * (2 * kStages + 3 + 2 * kQ) <= 192, "barriers overlap the control words");
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 192);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 196);
-  volatile int* tq = reinterpret_cast<volatile int*>(ctl + 208);  // [kQ] claimed tile ids
-  int* pfx = reinterpret_cast<int*>(ctl + 256);
-  float* stg_all = reinterpret_cast<float*>(pfx + (MOE_MAX_EXPERTS + 1) + 3);
+  static_assert(8 * (2 * kStages + 3 + 2 * kQ) <= 256, "barriers overlap the control words");
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 260);
+  volatile int* tq = reinterpret_cast<volatile int*>(ctl + 272);  // [kQ] claimed tile ids
+  int* pfx = reinterpret_cast<int*>(ctl + 320);                   // [E + 1], E + 1 <= Sh::kPfxCap
+  float* scl_all = reinterpret_cast<float*>(pfx + Sh::kPfxCap);   // FP8: [kEpiWarps][kScaleFloats]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -393,8 +405,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     __syncwarp();
   } else {
-    float* stg = stg_all + warp * 32 * kStagePitch;
-    float* scl = stg_all + kEpiWarps * 32 * kStagePitch + warp * kScaleFloats;  // [chunk 0..1][gate 32 | up 32]
+    float* scl = scl_all + warp * kScaleFloats;  // FP8: [chunk 0..1][gate 32 | up 32]
     const int quarter = warp & 3;       // TMEM lane quarter (rows 32*quarter ..)
     const int cpart = warp >> 2;        // column chunks [2*cpart, 2*cpart + 2) of each row half
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -461,25 +472,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               u[j + 3] = __float_as_uint(rs * b.w * __uint_as_float(u[j + 3]));
             }
           }
-          uint32_t* srow = reinterpret_cast<uint32_t*>(stg + lane * kStagePitch);
+          uint32_t hw[16];  // this lane's row: h columns c*32 .. c*32+31 as bf16 pairs
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
             const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
             const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
-            srow[j] = *reinterpret_cast<const uint32_t*>(&hv);
+            hw[j] = *reinterpret_cast<const uint32_t*>(&hv);
           }
-          __syncwarp();
+          // Lanes 2i and 2i+1 swap halves (one shuffle a word), so that each 32-byte store of
+          // a lane pair covers the 64 bytes of one row: a store instruction writes 16 whole
+          // row segments. Storing each lane's own row instead (32 rows an instruction) took
+          // the kernel 3 % longer, and staging through shared memory leaves no room for a
+          // seventh ring slot.
+          const bool odd = (lane & 1) != 0;
+          uint32_t lo[8], hi[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rl = i * 4 + (lane >> 3);
-            const int q = lane & 7;
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(stg + rl * kStagePitch) + 2 * q;
-            uint2* dst =
-                reinterpret_cast<uint2*>(args.h + static_cast<size_t>(rowbase + rl) * args.I + n0 + c * 32) + q;
-            *dst = make_uint2(src[0], src[1]);
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t got = __shfl_xor_sync(0xffffffffu, odd ? hw[k] : hw[8 + k], 1);
+            lo[k] = odd ? got : hw[k];      // row 2i, columns [16 odd, +16)
+            hi[k] = odd ? hw[8 + k] : got;  // row 2i+1, same columns
           }
-          __syncwarp();
+          __nv_bfloat16* dst =
+              args.h + static_cast<size_t>(rowbase + (lane & ~1)) * args.I + n0 + c * 32 + (odd ? 16 : 0);
+          ptx::st_b32x8(dst, lo);
+          ptx::st_b32x8(dst + args.I, hi);
         }
       }
       ptx::tc_fence_before();
@@ -498,12 +515,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 namespace {
 
+template <bool F8, int S>
+moe_status_t launch_gate_up_shape(const CUtensorMap& map_b, const pair::GemmArgs& a, cudaStream_t s) {
+  using Sh = pair::Shape<F8, S>;
+  if (a.E + 1 > Sh::kPfxCap) return MOE_ERR_UNSUPPORTED;
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(pair::moe_gate_up_kernel<F8, S>), static_cast<int>(Sh::kSmem)))
+    return MOE_ERR_CUDA;
+  return launch_pdl(pair::moe_gate_up_kernel<F8, S>, dim3(num_sms()), dim3(Sh::kThreads), Sh::kSmem, s, map_b, a);
+}
+
+// bf16: seven ring slots up to kDeepMaxExperts experts, six beyond (the full expert table
+// takes the seventh slot's room). The MMA waits on its operands' latency, so a deeper ring
+// runs faster: 210, 199 and 191 us with five, six and seven slots at T=4096, H=2048,
+// I=768, E=128, top-8. FP8 keeps six slots: its channel scales take the room of the seventh.
 template <bool F8>
 moe_status_t launch_gate_up(const CUtensorMap& map_b, const pair::GemmArgs& a, cudaStream_t s) {
-  using namespace pair;
-  if (!ensure_smem_attr(reinterpret_cast<const void*>(moe_gate_up_kernel<F8>), static_cast<int>(kGemmSmem)))
-    return MOE_ERR_CUDA;
-  return launch_pdl(moe_gate_up_kernel<F8>, dim3(num_sms()), dim3(kGemmThreads), kGemmSmem, s, map_b, a);
+  if (!F8 && a.E <= pair::kDeepMaxExperts) return launch_gate_up_shape<false, 7>(map_b, a, s);
+  return launch_gate_up_shape<F8, 6>(map_b, a, s);
 }
 
 }  // namespace

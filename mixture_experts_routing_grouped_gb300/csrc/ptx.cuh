@@ -120,6 +120,12 @@ __device__ __forceinline__ void st_f32x4(float* dst, float4 v, uint64_t pol) {
                "f"(v.z), "f"(v.w), "l"(pol)
                : "memory");
 }
+// 32-byte store (dst 32-byte aligned).
+__device__ __forceinline__ void st_b32x8(void* dst, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
 
 // ---------------------------------------------------------------- cp.async (gather)
 // 16-byte global->shared copy; src_bytes = 0 writes 16 zero bytes.
