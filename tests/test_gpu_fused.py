@@ -64,6 +64,9 @@ def test_tiny_layer():
                     topk_group=4, scoring="sigmoid", routed_scaling_factor=2.5, seed=13),
     synth.MoEConfig("skewed_T600_H512_I256_E4_top1_norenorm", T=600, H=512, I=256, E=4, topk=1, renormalize=False,
                     seed=14, logit_sigma=3.0),
+    # 256 experts on the 128-row kernels: the seven-slot bf16 gate_up instance at its table's limit
+    synth.MoEConfig("experts_at_limit_T2048_H256_I128_E256_top8", T=2048, H=256, I=128, E=256, topk=8,
+                    num_expert_group=8, topk_group=4, scoring="sigmoid", seed=16),
     # more than 256 experts on the 128-row kernels: the six-slot bf16 gate_up instance
     synth.MoEConfig("many_experts_T4096_H256_I128_E512_top8", T=4096, H=256, I=128, E=512, topk=8,
                     num_expert_group=8, topk_group=4, seed=15),
