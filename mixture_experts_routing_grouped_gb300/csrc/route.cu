@@ -602,10 +602,11 @@ __global__ void __launch_bounds__(kSegThreads, 6) grouped_topk_seg_kernel(const 
 // A persistent CTA per SM: one producer thread streams tiles of 32 tokens (their
 // [32, E] fp32 logits) into shared-memory stages with 2D tensor loads (boxes of 32
 // logits x 32 tokens, 128-byte swizzle, so that lane r reading its own row touches
-// eight distinct bank groups per quarter-warp), and six compute warps take the
+// eight distinct bank groups per quarter-warp), and seven compute warps take the
 // tiles in turn, lane r of a warp selecting for token r of its tile; each warp owns
 // its own stages. The loads of the next tiles are in flight while the current ones
-// are selected.
+// are selected. The selection's dependent chains bound the kernel, so the stages are
+// as many as shared memory holds (224 KB), for as many compute warps.
 //
 // Per token (GroupedTopK blog 3.2-3.6, on the logits as in its section 七):
 //  1. maxima of every unit of 8 consecutive experts, and the group maxima from them;
@@ -623,7 +624,7 @@ __global__ void __launch_bounds__(kSegThreads, 6) grouped_topk_seg_kernel(const 
 namespace tpt {
 
 constexpr int kTile = 32;
-constexpr int kComputeWarps = 6;
+constexpr int kComputeWarps = 7;
 constexpr int kThreads = (kComputeWarps + 1) * 32;
 constexpr int kK = 8;
 
@@ -634,12 +635,13 @@ struct Shape {
   static constexpr int kStageBytes = kTile * E * 4;     // 32 KB at E = 256
   // each compute warp owns kDepth stages (one consumer per stage: its barriers are waited on in
   // order by one warp, so no wait can match an older phase of the same parity)
-  static constexpr int kDepth = (192 * 1024) / kStageBytes / kComputeWarps > 0
-                                    ? (192 * 1024) / kStageBytes / kComputeWarps : 1;
+  static constexpr int kDepth = (224 * 1024) / kStageBytes / kComputeWarps > 0
+                                    ? (224 * 1024) / kStageBytes / kComputeWarps : 1;
   static constexpr int kStages = kComputeWarps * kDepth;
   static constexpr int kBarOff = kStages * kStageBytes;
-  static constexpr int kHistOff = kBarOff + 2 * kStages * 8 + 16;      // per-warp expert counts
-  static constexpr int kSmem = kHistOff + kComputeWarps * E * 4 + 1024;  // + alignment slack
+  static constexpr int kSmem = kBarOff + 2 * kStages * 8 + 16 + 1024;  // + alignment slack
+  static_assert(kSmem <= 232448, "routing stages exceed the per-CTA shared memory");
+  static_assert(E * 4 <= kStageBytes, "a tile's expert counts fit in its stage");
 };
 
 // Shared address of logit e of lane-row r in a stage (see the swizzle above).
@@ -852,7 +854,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_topk_tpt_kernel(const __g
       den = bs[0];
     }
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
+    // the stage is free once read, unless the tile's expert counts are taken in it below
+    if (!tile_hist && lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
 
     // 3.6: weights (one reciprocal of the sum; each sigmoid as the correctly rounded 1 / (1 + e^-x))
     float w[kK];
@@ -888,9 +891,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_topk_tpt_kernel(const __g
       ip[0] = make_int4(id[0], id[1], id[2], id[3]);
       ip[1] = make_int4(id[4], id[5], id[6], id[7]);
     }
-    // the tile's expert counts (align's first pass over these pairs), when asked for
+    // the tile's expert counts (align's first pass over these pairs), when asked for,
+    // counted in the warp's own stage (its logits are no longer read), which is then freed
     if (tile_hist) {
-      int* wh = reinterpret_cast<int*>(smem + S::kHistOff) + warp * E;
+      int* wh = reinterpret_cast<int*>(smem + s * S::kStageBytes);
       for (int e = lane; e < E; e += 32) wh[e] = 0;
       __syncwarp();
       if (token < T) {
@@ -903,7 +907,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_topk_tpt_kernel(const __g
       __syncwarp();
       int32_t* row_out = tile_hist + static_cast<size_t>(tile) * E;
       for (int e = lane; e < E; e += 32) row_out[e] = wh[e];
+      // the next tile's copy into this stage (async proxy) follows these shared-memory writes
+      ptx::fence_proxy_async_smem();
       __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar_empty + 8 * s);
     }
   }
 }

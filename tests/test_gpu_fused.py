@@ -64,6 +64,11 @@ def test_tiny_layer():
                     topk_group=4, scoring="sigmoid", routed_scaling_factor=2.5, seed=13),
     synth.MoEConfig("skewed_T600_H512_I256_E4_top1_norenorm", T=600, H=512, I=256, E=4, topk=1, renormalize=False,
                     seed=14, logit_sigma=3.0),
+    # from 8192 tokens the streaming routing kernel, which also writes each 32-token tile's
+    # expert counts for align
+    synth.MoEConfig("streamed_routing_T8192_H256_I128_E128_top8", T=8192, H=256, I=128, E=128, topk=8, seed=17),
+    synth.MoEConfig("streamed_routing_T8192_H256_I128_E256_G8_top8", T=8192, H=256, I=128, E=256, topk=8,
+                    num_expert_group=8, topk_group=4, scoring="sigmoid", seed=18),
     # 256 experts on the 128-row kernels: the seven-slot bf16 gate_up instance at its table's limit
     synth.MoEConfig("experts_at_limit_T2048_H256_I128_E256_top8", T=2048, H=256, I=128, E=256, topk=8,
                     num_expert_group=8, topk_group=4, scoring="sigmoid", seed=16),
