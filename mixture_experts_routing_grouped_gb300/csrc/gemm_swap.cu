@@ -353,7 +353,9 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
         cs0 = __ldg(sw + i);
         cs1 = __ldg(sw + args.a1_offset + i);
       }
-      if (!ptx::mbar_wait(tfull_bar(b), tph, abort_flag)) break;
+      // the four warps meet at named barriers in this loop, so they leave it together
+      const bool full = ptx::mbar_wait(tfull_bar(b), tph, abort_flag);
+      if (ptx::bar_any(1, 128, !full)) break;
       ptx::tc_fence_after();
       const uint32_t d0 = tmem_base + lane_off + b * 256, d1 = d0 + C::kD1Off;
       for (int c = 0; c * 32 < st.n; ++c) {

@@ -493,14 +493,20 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       // store for one token writes 32 consecutive channels of its output row.
       for (int it = 0;; ++it) {
         Task k;
-        if (!next_task(it, k)) break;
+        const bool got = next_task(it, k);
         const int b = it & 1;
         float* sc = scl + b * kLBN;
-        if (!second) sc[r] = r < k.rows ? __ldg(args.sx + k.row0 + r) : 0.f;
-        const float sw = __ldg(args.sw + static_cast<size_t>(k.e) * args.N + k.nt * kLBN + r);
+        float sw = 0.f;
+        if (got) {
+          if (!second) sc[r] = r < k.rows ? __ldg(args.sx + k.row0 + r) : 0.f;
+          sw = __ldg(args.sw + static_cast<size_t>(k.e) * args.N + k.nt * kLBN + r);
+        }
+        // the eight epilogue warps: scales staged; they leave the loop together (they meet
+        // at this named barrier every task)
+        if (ptx::bar_any(1, 256, !got)) break;
         const int chunks = min(kLBN / 64, max(0, (k.rows - c0 * 32 + 31) / 32));  // warp-uniform
-        asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight epilogue warps: scales staged
-        if (!ptx::mbar_wait(tfull_bar(b), (it >> 1) & 1, abort_flag)) break;
+        const bool full = ptx::mbar_wait(tfull_bar(b), (it >> 1) & 1, abort_flag);
+        if (ptx::bar_any(1, 256, !full)) break;
         ptx::tc_fence_after();
         uint32_t d[2][32];
         if (chunks > 0) ptx::tmem_ld32(tmem_base + lane_off + b * kLBN + c0 * 32, d[0]);
@@ -532,15 +538,21 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
     } else {
     for (int it = 0;; ++it) {
       Task k;
-      if (!next_task(it, k)) break;
+      const bool got = next_task(it, k);
       const int b = it & 1;
       float* sc = scl + b * kLBN;
-      if (!second) sc[r] = __ldg(args.sw + static_cast<size_t>(k.e) * args.N + k.nt * kLBN + r);
-      const bool valid = r < k.rows;
+      const bool valid = got && r < k.rows;
       const int row = k.row0 + r;
-      const float sx = valid ? __ldg(args.sx + row) : 0.f;
-      asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight epilogue warps: scales staged
-      if (!ptx::mbar_wait(tfull_bar(b), (it >> 1) & 1, abort_flag)) break;
+      float sx = 0.f;
+      if (got) {
+        if (!second) sc[r] = __ldg(args.sw + static_cast<size_t>(k.e) * args.N + k.nt * kLBN + r);
+        if (valid) sx = __ldg(args.sx + row);
+      }
+      // the eight epilogue warps: scales staged; they leave the loop together (they meet
+      // at this named barrier every task)
+      if (ptx::bar_any(1, 256, !got)) break;
+      const bool full = ptx::mbar_wait(tfull_bar(b), (it >> 1) & 1, abort_flag);
+      if (ptx::bar_any(1, 256, !full)) break;
       ptx::tc_fence_after();
       uint32_t d[2][32];
       ptx::tmem_ld32(tmem_base + lane_off + b * kLBN + c0 * 32, d[0]);

@@ -95,6 +95,21 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Named barrier `id` over `count` threads (a multiple of 32) that also tells each of them
+// whether any passed `pred` true. Threads that meet at a named barrier inside a loop take
+// the loop's exit on it, together: one that left alone (its bounded wait gave up while the
+// others' succeeded) would leave the rest waiting at the named barrier, which has no limit.
+__device__ __forceinline__ bool bar_any(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, %2, %3, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // ---------------------------------------------------------------- proxies / fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
