@@ -238,7 +238,8 @@ __global__ void __launch_bounds__(Shape<F8, S>::kThreads, 1)
   // its lanes, warp_wide) or by the single MMA thread.
   auto read_tile = [&](int j, int& t_out, bool warp_wide) -> bool {
     const int q = j % kQ;
-    const bool ok = ptx::mbar_wait(qfull_bar(q), static_cast<uint32_t>(j / kQ) & 1u, abort_flag);
+    bool ok = ptx::mbar_wait(qfull_bar(q), static_cast<uint32_t>(j / kQ) & 1u, abort_flag);
+    if (warp_wide) ok = __all_sync(0xffffffffu, ok);  // the warp goes on, or leaves, as one
     t_out = ok ? tq[q] : tiles;
     if (warp_wide) __syncwarp();
     if (ok && (!warp_wide || lane == 0)) ptx::mbar_arrive(qempty_bar(q));
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(Shape<F8, S>::kThreads, 1)
         }
         __syncwarp();
       }
-      if (!ptx::mbar_wait(tfull_bar, static_cast<uint32_t>(it) & 1u, abort_flag)) break;
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(tfull_bar, static_cast<uint32_t>(it) & 1u, abort_flag))) break;
       ptx::tc_fence_after();
       for (int half = 0; half < ti.nblk; ++half) {
         const uint32_t tbase = tmem_base + lane_off + half * kBN;

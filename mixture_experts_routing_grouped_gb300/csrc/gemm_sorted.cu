@@ -227,7 +227,8 @@ __global__ void __launch_bounds__(gemm_threads<F8>(), 1)
       if constexpr (F8) w *= valid ? __ldg(args.sa + pos) : 0.f;  // and the row's quantisation scale
       const int tok = valid ? sid / args.topk : -1;
       const int e_of_tile = F8 ? __ldg(args.expert_ids + mt) : 0;
-      if (!ptx::mbar_wait(tfull_bar(b), tphase, abort_flag)) break;
+      // the warp leaves as one (warp-wide TMEM loads and shuffles follow)
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(tfull_bar(b), tphase, abort_flag))) break;
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + lane_off + b * kBN;
       // Two forms of the combine loop, each the faster one measured for its operand type: the

@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(SwapCfg<NMAX>::kThreads, 1)
           __syncwarp();
         }
         const uint32_t use = static_cast<uint32_t>(g / C::kStages);
-        if (!ptx::mbar_wait(empty_bar(slot), (use & 1u) ^ 1u, abort_flag)) break;
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(empty_bar(slot), (use & 1u) ^ 1u, abort_flag))) break;
         if (lane == 0) {
           const int wrow = st.e * args.a_rows_per_expert + st.wb * args.wb_stride;
           ptx::mbar_arrive_expect_tx(full_bar(slot), 2 * kSwATile);

@@ -266,8 +266,8 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       report_error(args.err, MOE_DEVERR_GROUP_META);
     load_chunk();
     for (int it = 0;; ++it) {
-      if (it > 0 && !ptx::mbar_wait(taken_bar((it - 1) % kQ), static_cast<uint32_t>((it - 1) / kQ) & 1u,
-                                    abort_flag))
+      if (it > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(taken_bar((it - 1) % kQ),
+                                                             static_cast<uint32_t>((it - 1) / kQ) & 1u, abort_flag)))
         break;
       int t = static_cast<int>(blockIdx.x);
       if (it > 0 && lane == 0) t = static_cast<int>(gridDim.x) + atomicAdd(args.counter, 1);
@@ -391,9 +391,9 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
       bool ok = true;
       for (int it = 0; ok; ++it) {
         Task k;
-        if (!next_task(it, k)) break;
+        if (!__all_sync(0xffffffffu, next_task(it, k))) break;  // the warp goes on, or leaves, as one
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, ptx::mbar_wait(full_bar(stage), phase, abort_flag))) { ok = false; break; }
           const uint8_t* src = smem + stage * kTile8 + r * 128;
           uint4 v[4];
 #pragma unroll
@@ -408,7 +408,10 @@ __global__ void __launch_bounds__(lowp_threads<I8>(), 1)
             i8x4_to_f16x4(v[q].w, h[8 * q + 6], h[8 * q + 7]);
           }
           ptx::mbar_arrive(empty_bar(stage));
-          if (!ptx::mbar_wait(oempty_bar(ostage), ophase ^ 1u, abort_flag)) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, ptx::mbar_wait(oempty_bar(ostage), ophase ^ 1u, abort_flag))) {
+            ok = false;
+            break;
+          }
           ptx::tc_fence_after();
           ptx::tmem_st32(tmem_base + lane_off + kI8OpCol + ostage * (kLBK / 2) + half * 32, h);
           ptx::tmem_st_wait();

@@ -741,7 +741,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_topk_tpt_kernel(const __g
     const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
     if (tile >= ntiles) break;
     const int s = warp * S::kDepth + l % S::kDepth;
-    if (!ptx::mbar_wait(bar_full + 8 * s, (l / S::kDepth) & 1, abort_flag)) {
+    // the warp leaves as one (warp-wide shuffles and syncs follow)
+    if (!__all_sync(0xffffffffu, ptx::mbar_wait(bar_full + 8 * s, (l / S::kDepth) & 1, abort_flag))) {
       if (lane == 0) report_error(err, MOE_DEVERR_TIMEOUT);
       break;
     }
